@@ -1,0 +1,90 @@
+"""Shared test helpers: host copies of step inputs for the oracle, and an
+independent dense attention written with torch library ops."""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+PAGE = 128
+D = 128
+
+
+def q_bits(q: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bit patterns (host)."""
+    return q.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_problem(inp, oracle):
+    return oracle.Problem(q_bits(inp.q), inp.kv.detach().cpu().numpy(),
+                          inp.block_table.detach().cpu().numpy(),
+                          inp.seq_lens.detach().cpu().numpy(), inp.qlen, inp.num_q_heads,
+                          inp.num_kv_heads, inp.sm_scale, inp.k_scale, inp.v_scale)
+
+
+def read_golden_rows(name: str) -> np.ndarray:
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([int(v) for v in line.split()])
+    return np.array(rows, dtype=np.int64)
+
+
+def fp8_to_f64(kv_bytes: torch.Tensor) -> torch.Tensor:
+    """Decode fp8 bytes with torch's own float8_e4m3fn conversion."""
+    return kv_bytes.cpu().view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def dense_reference(inp, topk=None):
+    """Causal attention written with torch ops in fp64: for each request and KV
+    head, gather the logical key/value sequence through the block table, form
+    softmax(q K^T * sm_scale + causal mask) V over the listed pages (all
+    visible pages when topk is None).  Also returns, per (g, token, block), the
+    max over the group's heads of the visible logits (the block score)."""
+    B, Q = inp.batch, inp.qlen
+    Hq, Hkv = inp.num_q_heads, inp.num_kv_heads
+    G = Hq // Hkv
+    S = inp.stride
+    kvf = fp8_to_f64(inp.kv)
+    K_all = kvf[..., :D] * inp.k_scale
+    V_all = kvf[..., D:] * inp.v_scale
+    q = inp.q.cpu().to(torch.float64)
+    bt = inp.block_table.cpu()
+    out = torch.zeros((B * Q, Hq, D), dtype=torch.float64)
+    scores = torch.full((Hkv, B * Q, S), -math.inf, dtype=torch.float64)
+    for b, L in enumerate(inp.seq_lens_list):
+        n_pages = math.ceil(L / PAGE)
+        if n_pages == 0:
+            continue
+        pages = bt[b, :n_pages].long()
+        for g in range(Hkv):
+            K = K_all[pages, g].reshape(n_pages * PAGE, D)
+            V = V_all[pages, g].reshape(n_pages * PAGE, D)
+            for j in range(Q):
+                i = b * Q + j
+                pos = L - Q + j
+                if pos < 0:
+                    continue
+                qs = q[i, g * G:(g + 1) * G]                     # [G, D]
+                logits = (qs @ K.T) * inp.sm_scale               # [G, n_pages*128]
+                key_idx = torch.arange(n_pages * PAGE)
+                visible = key_idx <= pos
+                if topk is not None:
+                    sel = torch.zeros(n_pages, dtype=torch.bool)
+                    for n in topk[i, g].tolist():
+                        if n >= 0:
+                            sel[n] = True
+                    visible = visible & sel[key_idx // PAGE]
+                masked = logits.masked_fill(~visible, -math.inf)
+                blk = masked.reshape(G, n_pages, PAGE).amax(dim=(0, 2))
+                scores[g, i, :n_pages] = blk
+                if visible.any():
+                    p = torch.softmax(masked, dim=-1)
+                    out[i, g * G:(g + 1) * G] = p @ V
+    return out, scores
