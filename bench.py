@@ -1,0 +1,579 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse-decode step (score -> select -> attend -> merge).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints ONE JSON line.  A step is one pass of the whole decode step for one
+layer's batch: msa_score, msa_topk, msa_sparse_decode (+ msa_combine when
+split).  Inputs are synthetic and resident in HBM before the timed region; the
+layers rotate over independent KV pools whose total size is >= 4x the L2, so
+no step finds its inputs in L2.  The timed region is a CUDA-graph replay of
+the K steps with CUDA events recorded between the kernels on the launch
+stream.  value = query tokens / s (per layer, all ranks).
+
+--impl reference times the CPU oracle (the only reference implementation of
+this method available here) on the host cores: each step runs the oracle's
+whole pipeline for one (request, KV head) unit of the same workload.
+
+Under torchrun each rank runs an independent replica on its own GPU (the step
+has no exchange); rank 0 prints the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "sparse-decode query-tokens/s per layer"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-chunk", type=int, default=250)
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background; the
+    samples that arrive between mark_start() and mark_stop() are kept."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            target = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[device_index]
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    def summary(self):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [s for t, s in self.samples if self.t0 <= t <= self.t1]
+        where = "timed region"
+        if not inside:   # timed region shorter than the sampling period
+            inside = [s for t, s in self.samples if t >= self.t0 - 0.5][:3]
+            where = "nearest samples (timed region shorter than the sampling period)"
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            parts = [p.strip() for p in s.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": where}
+
+
+def _source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_gqa_score_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"attend": ("msa_attend.cu", "msa_device.cuh"),
+                  "score": ("msa_score.cu", "msa_device.cuh"),
+                  "topk": ("msa_topk.cu",)}
+
+
+def _traffic_from_profiles(stage: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, or None
+    when absent or taken on different kernel source."""
+    path = os.path.join(PROFILES, f"{stage}_kernel_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_digest") != _source_digest(*KERNEL_SOURCES[stage]):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def _work(inp, topk_cpu: np.ndarray | None):
+    """Algorithmic bytes per launch of each stage (the figures the design doc defines)."""
+    B, Q, Hq, Hkv, S = inp.batch, inp.qlen, inp.num_q_heads, inp.num_kv_heads, inp.stride
+    T = B * Q
+    pages = [math.ceil(L / 128) for L in inp.seq_lens_list]
+    q_bytes = T * Hq * 128 * 2
+    score = sum(pages) * Hkv * 16384 + q_bytes + Hkv * T * S * 4 + B * S * 4
+    cand = 0
+    for b, L in enumerate(inp.seq_lens_list):
+        for j in range(Q):
+            pos = L - Q + j
+            if pos >= 0:
+                cur = pos // 128
+                cand += cur if cur + 1 > 16 else 0
+    topk = cand * Hkv * 4 + T * Hkv * 16 * 4
+    union = per_token = 0
+    if topk_cpu is not None:
+        for b in range(B):
+            rows = topk_cpu[b * Q:(b + 1) * Q]          # [Q, Hkv, 16]
+            for g in range(Hkv):
+                ids = rows[:, g, :]
+                ids = ids[ids >= 0]
+                union += len(np.unique(ids))
+                per_token += len(ids)
+    attend = union * 32768 + 2 * q_bytes + T * Hkv * 16 * 4
+    return {"score": score, "topk": topk, "attend": attend, "union_pages": union,
+            "token_pages": per_token, "attend_kv_bytes": union * 32768}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from block_sparse_gqa_score_gb300 import workloads as wl
+    name = args.workload or wl.HEADLINE
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device="cpu")
+    p = _problem(inp, oracle)
+    cores = oracle.default_threads()
+    units = [(b, g) for b in range(inp.batch) for g in range(inp.num_kv_heads)
+             if inp.seq_lens_list[b] > 0]
+
+    given = inp.topk.numpy() if w.topk_given else None
+
+    def step(k):
+        b, g = units[k % len(units)]
+        _oracle_unit(p, inp, oracle, b, g, cores, given)
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(args.warmup + k)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * inp.qlen / inp.num_kv_heads
+    v = tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": w.describe(),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one (request, KV head) unit per step, round robin: "
+                                       + ("attention of its query rows x 16 heads over the "
+                                          "given top-k" if w.topk_given else
+                                          "scores of all its visible blocks, selection of its "
+                                          "query rows, attention of its query rows x 16 heads")
+                                       + "; counted as qlen/Hkv query tokens"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def _problem(inp, oracle):
+    return oracle.Problem(inp.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16),
+                          inp.kv.cpu().numpy(), inp.block_table.cpu().numpy(),
+                          inp.seq_lens.cpu().numpy(), inp.qlen, inp.num_q_heads,
+                          inp.num_kv_heads, inp.sm_scale, inp.k_scale, inp.v_scale)
+
+
+def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
+    """The oracle's whole pipeline for one (request, KV head) unit."""
+    Q, G = inp.qlen, inp.num_q_heads // inp.num_kv_heads
+    L = inp.seq_lens_list[b]
+    cur = (L - 1) // 128
+    if topk_given is None:
+        triples = [(b, g, n) for n in range(cur + 1)]
+        s = oracle.score_blocks(p, triples, nthreads)
+        sub = np.where(np.isnan(s[g:g + 1, b * Q:(b + 1) * Q]), -np.inf,
+                       s[g:g + 1, b * Q:(b + 1) * Q])
+        t = oracle.topk(sub, np.array([L], dtype=np.int32), Q)       # [Q, 1, 16]
+        full = np.full((inp.tokens, inp.num_kv_heads, 16), -1, dtype=np.int32)
+        full[b * Q:(b + 1) * Q, g] = t[:, 0]
+    else:
+        full = topk_given
+    rows = [(b * Q + j) * inp.num_q_heads + g * G + h for j in range(Q) for h in range(G)]
+    oracle.attend_rows(p, full, rows, nthreads)
+
+
+def cpu_baseline(inp, w, topk_cpu, budget_s: float = 12.0):
+    """The oracle timed on this host on a bounded sample of the workload."""
+    import oracle
+    p = _problem(inp, oracle)
+    cores = oracle.default_threads()
+    units = [(b, g) for b in range(inp.batch) for g in range(inp.num_kv_heads)
+             if inp.seq_lens_list[b] > 0]
+    done = 0
+    t0 = time.perf_counter()
+    for b, g in units:
+        _oracle_unit(p, inp, oracle, b, g, cores, topk_cpu if w.topk_given else None)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    tokens = done * inp.qlen / inp.num_kv_heads
+    sample = (f"{done} of {len(units)} (request, KV head) units of layer 0, each the whole "
+              f"oracle pipeline ({'attend only, given top-k' if w.topk_given else 'score, select, attend'})")
+    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds": dt}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import block_sparse_gqa_score_gb300 as msa
+    from block_sparse_gqa_score_gb300 import build as msa_build
+    from block_sparse_gqa_score_gb300 import workloads as wl
+
+    msa_build.build()
+    msa._native.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    name = args.workload or wl.HEADLINE
+    w = wl.WORKLOADS[name]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+
+    # layers: independent KV pools, total >= 4x L2, at least 2
+    first = wl.make_inputs(w, device=dev, layer=0)
+    layer_bytes = first.kv.numel() + first.q.numel() * 2
+    n_layers = max(2, math.ceil(4 * l2 / max(layer_bytes, 1)))
+    layers = [first] + [wl.make_inputs(w, device=dev, layer=l) for l in range(1, n_layers)]
+    splits = msa.choose_splits(w.batch, w.qlen, w.num_kv_heads, props.multi_processor_count)
+    bufs = [msa.DecodeBuffers.allocate(w.batch, w.qlen, w.num_q_heads, w.num_kv_heads,
+                                       inp.stride, dev, splits) for inp in layers]
+    stream = torch.cuda.Stream(dev)
+
+    def stage_calls(l):
+        inp, bf = layers[l], bufs[l]
+        if w.topk_given:
+            return [lambda: None, lambda: None,
+                    lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                              inp.topk, inp.qlen, inp.sm_scale, inp.k_scale,
+                                              inp.v_scale, out=bf.out, num_splits=bf.num_splits,
+                                              workspace=bf.workspace)]
+        return [lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
+                                  inp.sm_scale, inp.k_scale, scores=bf.scores),
+                lambda: msa.topk(bf.scores, inp.seq_lens, inp.qlen, out=bf.topk),
+                lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk,
+                                          inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
+                                          out=bf.out, num_splits=bf.num_splits,
+                                          workspace=bf.workspace)]
+
+    launches_per_step = (1 if w.topk_given else 3) + (1 if splits > 1 else 0)
+
+    # warm-up (eager), then the per-layer work figures from the real top-k lists
+    msa.get_error(clear=True)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            for f in stage_calls(k % n_layers):
+                f()
+    torch.cuda.synchronize(dev)
+    flags = msa.get_error(clear=True)
+    works = [_work(inp, (inp.topk if w.topk_given else bf.topk).cpu().numpy())
+             for inp, bf in zip(layers, bufs)]
+
+    # graph of `chunk` steps with timing events between the stages
+    chunk = max(1, min(args.steps, args.graph_chunk))
+    graphs = []
+    mode = "cuda-graph"
+    try:
+        def capture(nsteps, offset):
+            g = torch.cuda.CUDAGraph()
+            evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                   for _ in range(nsteps)]
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(nsteps):
+                    calls = stage_calls((offset + k) % n_layers)
+                    evs[k][0].record()
+                    calls[0]()
+                    evs[k][1].record()
+                    calls[1]()
+                    evs[k][2].record()
+                    calls[2]()
+                    evs[k][3].record()
+            return g, evs
+        full, rem = divmod(args.steps, chunk)
+        if full:
+            graphs.append((capture(chunk, 0), full))
+        if rem:
+            graphs.append((capture(rem, 0), 1))
+        for (g, _), _n in graphs:      # one untimed pass: graph upload
+            g.replay()
+        torch.cuda.synchronize(dev)
+    except Exception as e:  # pragma: no cover - depends on the torch build
+        mode = f"eager ({type(e).__name__})"
+        graphs = []
+
+    clocks = ClockSampler(local)
+    time.sleep(0.2)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eager_evs = []
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    start.record(stream)
+    if graphs:
+        for (g, _evs), reps in graphs:
+            for _ in range(reps):
+                g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                calls = stage_calls(k % n_layers)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                for s_i in range(3):
+                    ev[s_i].record()
+                    calls[s_i]()
+                ev[3].record()
+                eager_evs.append(ev)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_stop()
+    _barrier(world)
+    total_ms = _max_over_ranks(start.elapsed_time(stop), world)
+    flags |= msa.get_error(clear=True)
+
+    # per-stage average durations (last graph pass, or every eager step)
+    ev_lists = graphs[0][0][1] if graphs else eager_evs
+    stage_ms = {"score": [], "topk": [], "attend": []}
+    for ev in ev_lists:
+        stage_ms["score"].append(ev[0].elapsed_time(ev[1]))
+        stage_ms["topk"].append(ev[1].elapsed_time(ev[2]))
+        stage_ms["attend"].append(ev[2].elapsed_time(ev[3]))
+    avg_ms = {k: (sum(v) / len(v) if v else 0.0) for k, v in stage_ms.items()}
+    T = w.tokens
+    value = world * T * args.steps / (total_ms / 1e3)
+    peak, peak_kind = _peaks()
+    mean_work = {k: sum(x[k] for x in works) / len(works) for k in works[0]}
+    stages = {}
+    for k in ("score", "topk", "attend"):
+        if w.topk_given and k != "attend":
+            continue
+        gbs = mean_work[k] / (avg_ms[k] / 1e3) / 1e9 if avg_ms[k] > 0 else None
+        stages[k] = {"ms": avg_ms[k], "algorithmic_bytes": mean_work[k], "GB/s": gbs,
+                     "frac_of_hbm": (gbs / peak) if gbs else None}
+    dominant = max(stages, key=lambda k: stages[k]["ms"])
+    d = stages[dominant]
+    roofline = {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": d["GB/s"],
+                "peak": peak, "unit": "GB/s", "frac": d["frac_of_hbm"],
+                "traffic": _traffic_from_profiles(dominant, name), "peak_kind": peak_kind,
+                "note": f"of {peak_kind}; achieved = algorithmic bytes per launch / mean "
+                        "CUDA-event duration in the timed region"}
+    att = stages["attend"]
+    gathered = {"GB/s": mean_work["attend_kv_bytes"] / (avg_ms["attend"] / 1e3) / 1e9,
+                "union_pages_per_step": mean_work["union_pages"],
+                "token_pages_per_step": mean_work["token_pages"]}
+    gathered["frac_of_hbm"] = gathered["GB/s"] / peak
+
+    line = {"impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8e4m3 KV, f16 MMA, f32 accumulate", "data": "synthetic",
+            "config": dict(w.describe(), layers_rotated=n_layers,
+                           l2_policy=f"inputs larger than L2: {n_layers} independent layers "
+                                     f"({layer_bytes * n_layers / 1e9:.2f} GB) rotated",
+                           splits=splits, timing=mode, parallelism=f"replicas x{world}"),
+            "roofline": roofline, "stages": stages, "attend_gathered_kv": gathered,
+            "gpu_launches": launches_per_step * args.steps, "error_flags": flags}
+    line["clocks"] = clocks.summary()
+
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = _e2e(msa, w, layers, bufs, stream, dev, world, args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp0 = layers[0]
+        tk = (inp0.topk if w.topk_given else bufs[0].topk).cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline(_to_cpu(inp0), w, tk)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def _to_cpu(inp):
+    import copy
+    c = copy.copy(inp)
+    c.q, c.kv, c.block_table, c.seq_lens = (inp.q.cpu(), inp.kv.cpu(), inp.block_table.cpu(),
+                                            inp.seq_lens.cpu())
+    c.topk = inp.topk.cpu() if inp.topk is not None else None
+    return c
+
+
+def _e2e(msa, w, layers, bufs, stream, dev, world, args):
+    """The same metric through the public Python API, with each step's inputs
+    (q, seq_lens, block_table, and the given top-k for attend-only workloads)
+    copied from pinned host memory and the output copied back; the KV cache is
+    resident model state."""
+    n_layers = len(layers)
+    host = []
+    for inp in layers:
+        h = {"q": inp.q.cpu().pin_memory(), "seq_lens": inp.seq_lens.cpu().pin_memory(),
+             "block_table": inp.block_table.cpu().pin_memory()}
+        if w.topk_given:
+            h["topk"] = inp.topk.cpu().pin_memory()
+        h["out"] = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
+        host.append(h)
+    dq = [torch.empty_like(inp.q) for inp in layers]
+    dsl = [torch.empty_like(inp.seq_lens) for inp in layers]
+    dbt = [torch.empty_like(inp.block_table) for inp in layers]
+    dtk = [torch.empty_like(inp.topk) if w.topk_given else None for inp in layers]
+    h2d = host[0]["q"].numel() * 2 + host[0]["seq_lens"].numel() * 4 + \
+        host[0]["block_table"].numel() * 4 + (host[0]["topk"].numel() * 4 if w.topk_given else 0)
+    d2h = host[0]["out"].numel() * 2
+    steps = min(args.steps, 500)
+
+    def one(k):
+        l = k % n_layers
+        inp, bf, h = layers[l], bufs[l], host[l]
+        dq[l].copy_(h["q"], non_blocking=True)
+        dsl[l].copy_(h["seq_lens"], non_blocking=True)
+        dbt[l].copy_(h["block_table"], non_blocking=True)
+        if w.topk_given:
+            dtk[l].copy_(h["topk"], non_blocking=True)
+            msa.sparse_decode(dq[l], inp.kv, dbt[l], dsl[l], dtk[l], inp.qlen, inp.sm_scale,
+                              inp.k_scale, inp.v_scale, out=bf.out, num_splits=bf.num_splits,
+                              workspace=bf.workspace)
+        else:
+            msa.decode_step(dq[l], inp.kv, dbt[l], dsl[l], inp.qlen, inp.sm_scale, inp.k_scale,
+                            inp.v_scale, buffers=bf)
+        h["out"].copy_(bf.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(min(args.warmup, 20)):
+            one(k)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in range(steps):
+            one(k)
+        b.record()
+        torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    return {"value": world * w.tokens * steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps, "path": "public Python API, eager launches"}
+
+
+def main():
+    args = _args()
+    rank, world, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+"""GB300-native (sm_103a) block-sparse GQA decode over a paged fp8 KV cache.
+
+One decode step of MiniMax-M3-style indexer-selected sparse attention, as the
+vLLM MiniMax-M3 sparse attention pages and TensorRT-LLM PR #17171 describe it:
+
+  score()          per-block causal max of scaled q.k over each KV head's group
+  topk()           top-16 blocks (current block kept, ties to the lower index)
+  sparse_decode()  split-K attention over the selected pages (+ merge)
+  combine()        merge of split-K partials
+  decode_step()    the three stages back to back on one stream
+
+Every function here only checks and marshals torch tensors into the C ABI of
+libmsa.so (include/msa.h); all arithmetic runs in that library's CUDA kernels.
+There is no CPU fallback: if the library is missing, calls raise.
+
+Tensor layouts (see include/msa.h): q bf16 [T, Hq, 128] with T = B * qlen
+request-major; kv fp8 e4m3 [num_blocks, Hkv, 128, 256] (K bytes 0..127, V bytes
+128..255), given as uint8 or float8_e4m3fn; block_table int32 [B, S];
+seq_lens int32 [B]; scores fp32 [Hkv, T, S]; topk int32 [T, Hkv, 16].
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _native
+from ._native import MSAError  # noqa: F401
+
+HEAD_DIM = 128
+PAGE_SIZE = 128
+TOPK = 16
+GROUP = 16
+MAX_QLEN = 32
+
+__all__ = ["score", "topk", "sparse_decode", "combine", "decode_step", "workspace_bytes",
+           "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
+
+
+def _lib():
+    return _native.load()
+
+
+def _stream(device: torch.device, stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+_KV_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _geometry(q, kv, block_table, seq_lens, qlen):
+    _need(q, "q", (torch.bfloat16,))
+    dev = q.device
+    _need(kv, "kv", _KV_DTYPES, dev)
+    _need(block_table, "block_table", (torch.int32,), dev)
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    if kv.dim() != 4 or kv.shape[2] != PAGE_SIZE or kv.shape[3] != 2 * HEAD_DIM:
+        raise ValueError("kv must be [num_blocks, Hkv, 128, 256]")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be [T, Hq, 128]")
+    if block_table.dim() != 2 or seq_lens.dim() != 1 or block_table.shape[0] != seq_lens.shape[0]:
+        raise ValueError("block_table must be [B, S] and seq_lens [B]")
+    B, S = block_table.shape
+    Hkv = kv.shape[1]
+    Hq = q.shape[1]
+    if q.shape[0] != B * qlen:
+        raise ValueError(f"q has {q.shape[0]} tokens, expected B*qlen = {B * qlen}")
+    return dev, int(B), int(S), int(Hq), int(Hkv), int(kv.shape[0])
+
+
+def workspace_bytes(batch: int, qlen: int, num_q_heads: int, num_splits: int) -> int:
+    return int(_lib().msa_workspace_bytes(batch, qlen, num_q_heads, num_splits))
+
+
+def choose_splits(batch: int, qlen: int, num_kv_heads: int, sm_count: int | None = None) -> int:
+    if sm_count is None:
+        sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(_lib().msa_choose_splits(batch, qlen, num_kv_heads, sm_count))
+
+
+def score(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
+          scores: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Block scores fp32 [Hkv, T, S] (msa_score)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    if scores is None:
+        scores = torch.empty((Hkv, B * qlen, S), dtype=torch.float32, device=dev)
+    _need(scores, "scores", (torch.float32,), dev)
+    if tuple(scores.shape) != (Hkv, B * qlen, S):
+        raise ValueError("scores must be [Hkv, T, S]")
+    st = _lib().msa_score(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+                          scores.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
+                          float(k_scale), _stream(dev, stream))
+    _native.check(st, "msa_score")
+    return scores
+
+
+def topk(scores: torch.Tensor, seq_lens: torch.Tensor, qlen: int, k: int = TOPK,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Selected blocks int32 [T, Hkv, 16] (msa_topk).  `scores` is indexed
+    [g, i, n] and may be any strided view (e.g. a transpose of [Hkv, S, T])."""
+    if not (isinstance(scores, torch.Tensor) and scores.is_cuda and scores.dtype == torch.float32):
+        raise TypeError("scores must be a CUDA float32 tensor")
+    dev = scores.device
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    Hkv, T, S = scores.shape
+    B = seq_lens.shape[0]
+    if T != B * qlen:
+        raise ValueError("scores' token dim must be B*qlen")
+    if out is None:
+        out = torch.empty((T, Hkv, k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    sh, stt, sn = scores.stride()
+    st = _lib().msa_topk(scores.data_ptr(), sh, stt, sn, seq_lens.data_ptr(), out.data_ptr(), B,
+                         qlen, Hkv, S, k, _stream(dev, stream))
+    _native.check(st, "msa_topk")
+    return out
+
+
+def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: float,
+                  k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
+                  num_splits: int = 0, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Attention over the selected pages, bf16 [T, Hq, 128] (msa_sparse_decode;
+    with more than one split the merge runs on the same stream)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    _need(topk_idx, "topk", (torch.int32,), dev)
+    if tuple(topk_idx.shape) != (B * qlen, Hkv, TOPK):
+        raise ValueError("topk must be [T, Hkv, 16]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,), dev)
+    splits = num_splits if num_splits > 0 else choose_splits(B, qlen, Hkv)
+    need = workspace_bytes(B, qlen, Hq, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib().msa_sparse_decode(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(),
+                                  seq_lens.data_ptr(), topk_idx.data_ptr(), ws_ptr, ws_bytes,
+                                  out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
+                                  float(k_scale), float(v_scale), splits, _stream(dev, stream))
+    _native.check(st, "msa_sparse_decode")
+    return out
+
+
+def combine(workspace: torch.Tensor, tokens: int, num_q_heads: int, num_splits: int,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Merge split-K partials (layout of msa_workspace_bytes) into bf16 [T, Hq, 128]."""
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda):
+        raise TypeError("workspace must be a CUDA tensor")
+    dev = workspace.device
+    if out is None:
+        out = torch.empty((tokens, num_q_heads, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    st = _lib().msa_combine(workspace.data_ptr(), out.data_ptr(), tokens, num_q_heads, num_splits,
+                            _stream(dev, stream))
+    _native.check(st, "msa_combine")
+    return out
+
+
+@dataclass
+class DecodeBuffers:
+    """Preallocated outputs and workspace of one decode step (reusable, and
+    stable addresses for CUDA-graph capture)."""
+    scores: torch.Tensor
+    topk: torch.Tensor
+    out: torch.Tensor
+    workspace: torch.Tensor | None
+    num_splits: int
+
+    @staticmethod
+    def allocate(batch: int, qlen: int, num_q_heads: int, num_kv_heads: int, stride: int,
+                 device, num_splits: int = 0) -> "DecodeBuffers":
+        T = batch * qlen
+        splits = num_splits if num_splits > 0 else choose_splits(batch, qlen, num_kv_heads)
+        need = workspace_bytes(batch, qlen, num_q_heads, splits)
+        ws = torch.empty(need, dtype=torch.uint8, device=device) if need else None
+        return DecodeBuffers(
+            scores=torch.empty((num_kv_heads, T, stride), dtype=torch.float32, device=device),
+            topk=torch.empty((T, num_kv_heads, TOPK), dtype=torch.int32, device=device),
+            out=torch.empty((T, num_q_heads, HEAD_DIM), dtype=torch.bfloat16, device=device),
+            workspace=ws, num_splits=splits)
+
+
+def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
+                v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None):
+    """score -> topk -> sparse_decode (-> combine) on one stream, no host sync.
+    Returns (scores, topk, out)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    if buffers is None:
+        buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
+    score(q, kv, block_table, seq_lens, qlen, sm_scale, k_scale, scores=buffers.scores,
+          stream=stream)
+    topk(buffers.scores, seq_lens, qlen, out=buffers.topk, stream=stream)
+    sparse_decode(q, kv, block_table, seq_lens, buffers.topk, qlen, sm_scale, k_scale, v_scale,
+                  out=buffers.out, num_splits=buffers.num_splits, workspace=buffers.workspace,
+                  stream=stream)
+    return buffers.scores, buffers.topk, buffers.out
+
+
+def get_error(clear: bool = True) -> int:
+    """The device's sticky MSA_ERR_* bits (synchronises the device)."""
+    flags = ctypes.c_uint(0)
+    _native.check(_lib().msa_get_error(ctypes.byref(flags), 1 if clear else 0), "msa_get_error")
+    return int(flags.value)

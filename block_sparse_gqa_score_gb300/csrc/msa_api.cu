@@ -1,0 +1,265 @@
+// msa_api.cu -- the extern "C" entry points declared in include/msa.h: host-side
+// argument validation, per-device set-up (SM count, the device error word),
+// TMA tensor-map encoding for the fp8 cache, and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "msa.h"
+#include "msa_launch.h"
+
+// Sticky per-device error word: kernels OR MSA_ERR_* bits into it.
+__device__ unsigned int msa_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 16;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  unsigned* err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Set-up for the current device, done once: resolves the device address of the
+// error word, reads the SM count and fetches the tensor-map encoder.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSA_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    void* err = nullptr;
+    if (cudaGetSymbolAddress(&err, msa_error_word) != cudaSuccess) return MSA_ECUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MSA_ECUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return MSA_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.err = static_cast<unsigned*>(err);
+    st.sm_count = sms;
+    st.ready = true;
+  }
+  *out = &st;
+  return MSA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+
+// Shape checks shared by the scorer and the attend.
+int check_common(const void* q, const void* kv, const int32_t* block_table,
+                 const int32_t* seq_lens, int B, int Q, int Hq, int Hkv, int S,
+                 int64_t num_blocks) {
+  if (B < 0 || B > 65535 || Q < 1 || Q > MSA_MAX_QLEN || Hkv < 1 || Hkv > 65535 ||
+      Hq != MSA_GROUP * Hkv || S < 1 || num_blocks < 1)
+    return MSA_EINVAL;
+  if (static_cast<int64_t>(B) * Q > INT_MAX / 4 || static_cast<int64_t>(B) * S > INT_MAX)
+    return MSA_EINVAL;
+  // TMA row coordinates (page * Hkv + g) * 128 must fit in int32
+  if (num_blocks * Hkv * MSA_PAGE_SIZE >= (static_cast<int64_t>(1) << 31)) return MSA_EINVAL;
+  if (!q || !kv || !block_table || !seq_lens) return MSA_EINVAL;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return MSA_EINVAL;
+  return MSA_OK;
+}
+
+// 2-D view of the cache as [num_blocks * Hkv * 128 rows, 256 bytes], read in
+// 128 x 128-byte boxes (one K or V half of a page-head) with 128B swizzling.
+int encode_kv_map(const void* kv, int Hkv, int64_t num_blocks, CUtensorMap* map) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2),
+                        static_cast<cuuint64_t>(num_blocks) * Hkv * MSA_PAGE_SIZE};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2)};
+  cuuint32_t box[2] = {MSA_HEAD_DIM, MSA_PAGE_SIZE};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_EINVAL;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int msa_version(void) { return 100; }
+
+const char* msa_strerror(int status) {
+  switch (status) {
+    case MSA_OK: return "ok";
+    case MSA_EINVAL: return "invalid argument (size, null or misaligned pointer)";
+    case MSA_ECUDA: return "CUDA runtime error";
+    case MSA_ENOSPC: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+size_t msa_workspace_bytes(int B, int Q, int Hq, int num_splits) {
+  if (B < 0 || Q < 1 || Hq < 1 || num_splits < 0 || num_splits > kMaxSplits) return 0;
+  if (num_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Q * Hq;
+  return static_cast<size_t>(num_splits) * rows * (MSA_HEAD_DIM + 2) * sizeof(float);
+}
+
+int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
+  if (B < 1 || Q < 1 || Hkv < 1 || sm_count < 1) return 1;
+  const int64_t units = static_cast<int64_t>(B) * Q * Hkv;  // one CTA per (token, KV head)
+  const int64_t slots = 2 * static_cast<int64_t>(sm_count);  // two CTAs per SM
+  if (units * 4 >= slots * 3) return 1;
+  int64_t s = (slots + units - 1) / units;
+  if (s > 8) s = 8;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+int msa_score(const void* q, const void* kv, const int32_t* block_table, const int32_t* seq_lens,
+              float* scores, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
+              float sm_scale, float k_scale, msa_stream_t stream) {
+  int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
+  if (st != MSA_OK) return st;
+  if (!scores || !aligned(scores, 4) || !finite_pos(sm_scale) || !finite_pos(k_scale))
+    return MSA_EINVAL;
+  if (B == 0) return MSA_OK;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != MSA_OK) return st;
+  CUtensorMap map;
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
+  msa::ScoreParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.scores = scores;
+  p.err = dev->err;
+  p.B = B;
+  p.Q = Q;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.chunk = (Q <= 4) ? 16 : 32;
+  p.num_blocks = num_blocks;
+  p.scale = sm_scale * k_scale;
+  return from_cuda(msa::launch_score(map, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_topk(const float* scores, int64_t stride_h, int64_t stride_t, int64_t stride_n,
+             const int32_t* seq_lens, int32_t* topk, int B, int Q, int Hkv, int S, int k,
+             msa_stream_t stream) {
+  if (k != MSA_TOPK || B < 0 || Q < 1 || Q > MSA_MAX_QLEN || Hkv < 1 || S < 1) return MSA_EINVAL;
+  if (static_cast<int64_t>(B) * Q * Hkv > INT_MAX / 2) return MSA_EINVAL;
+  if (!scores || !seq_lens || !topk || !aligned(scores, 4) || !aligned(seq_lens, 4) ||
+      !aligned(topk, 4))
+    return MSA_EINVAL;
+  if (B == 0) return MSA_OK;
+  DeviceState* dev;
+  int st = device_state(&dev);
+  if (st != MSA_OK) return st;
+  msa::TopkParams p{};
+  p.scores = scores;
+  p.stride_h = stride_h;
+  p.stride_t = stride_t;
+  p.stride_n = stride_n;
+  p.seq_lens = seq_lens;
+  p.topk = topk;
+  p.err = dev->err;
+  p.B = B;
+  p.Q = Q;
+  p.Hkv = Hkv;
+  p.S = S;
+  return from_cuda(msa::launch_topk(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_combine(const void* workspace, void* out, int T, int Hq, int num_splits,
+                msa_stream_t stream) {
+  if (T < 0 || Hq < 1 || num_splits < 1 || num_splits > kMaxSplits) return MSA_EINVAL;
+  if (!workspace || !out || !aligned(workspace, 16) || !aligned(out, 16)) return MSA_EINVAL;
+  if (T == 0) return MSA_OK;
+  const int64_t rows = static_cast<int64_t>(T) * Hq;
+  const float* part_o = static_cast<const float*>(workspace);
+  const float* part_ml = part_o + static_cast<int64_t>(num_splits) * rows * MSA_HEAD_DIM;
+  return from_cuda(msa::launch_combine(part_o, part_ml, static_cast<uint16_t*>(out), rows,
+                                       num_splits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_sparse_decode(const void* q, const void* kv, const int32_t* block_table,
+                      const int32_t* seq_lens, const int32_t* topk, void* workspace,
+                      size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                      int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                      int num_splits, msa_stream_t stream) {
+  int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
+  if (st != MSA_OK) return st;
+  if (!topk || !out || !aligned(topk, 4) || !aligned(out, 16) || !finite_pos(sm_scale) ||
+      !finite_pos(k_scale) || !std::isfinite(v_scale) || num_splits < 0 ||
+      num_splits > kMaxSplits)
+    return MSA_EINVAL;
+  if (B == 0) return MSA_OK;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != MSA_OK) return st;
+  const int splits = num_splits == 0 ? msa_choose_splits(B, Q, Hkv, dev->sm_count) : num_splits;
+  const size_t need = msa_workspace_bytes(B, Q, Hq, splits);
+  if (splits > 1 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
+    return MSA_ENOSPC;
+  CUtensorMap map;
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
+  const int64_t rows = static_cast<int64_t>(B) * Q * Hq;
+  msa::AttendParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.topk = topk;
+  p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.part_ml = splits > 1 ? static_cast<float*>(workspace) + splits * rows * MSA_HEAD_DIM : nullptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.err = dev->err;
+  p.B = B;
+  p.Q = Q;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.splits = splits;
+  p.num_blocks = num_blocks;
+  p.logit_scale = sm_scale * k_scale * 1.4426950408889634f;
+  p.v_scale = v_scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = from_cuda(msa::launch_attend(map, p, s))) != MSA_OK) return st;
+  if (splits > 1)
+    return from_cuda(
+        msa::launch_combine(p.part_o, p.part_ml, static_cast<uint16_t*>(out), rows, splits, s));
+  return MSA_OK;
+}
+
+int msa_get_error(unsigned int* flags, int clear) {
+  DeviceState* dev;
+  int st = device_state(&dev);
+  if (st != MSA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MSA_ECUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ECUDA;
+  if (flags) *flags = v;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MSA_ECUDA;
+  }
+  return MSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// msa_launch.h -- parameter blocks and host launchers of the sm_103a kernels
+// (internal to the library; the public interface is include/msa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace msa {
+
+struct ScoreParams {
+  const uint16_t* q;           // bf16 bits [T, Hq, 128]
+  const int32_t* block_table;  // [B, S]
+  const int32_t* seq_lens;     // [B]
+  float* scores;               // [Hkv, T, S]
+  unsigned* err;               // device error word
+  int B, Q, Hq, Hkv, S;
+  int chunk;                   // logical blocks per CTA
+  int64_t num_blocks;
+  float scale;                 // sm_scale * k_scale
+};
+
+struct TopkParams {
+  const float* scores;
+  int64_t stride_h, stride_t, stride_n;  // element strides of scores[g, i, n]
+  const int32_t* seq_lens;
+  int32_t* topk;                         // [T, Hkv, 16]
+  unsigned* err;
+  int B, Q, Hkv, S;
+};
+
+struct AttendParams {
+  const uint16_t* q;           // bf16 bits [T, Hq, 128]
+  const int32_t* block_table;  // [B, S]
+  const int32_t* seq_lens;     // [B]
+  const int32_t* topk;         // [T, Hkv, 16]
+  float* part_o;               // [splits, T, Hq, 128]     (splits > 1)
+  float* part_ml;              // [splits, T, Hq, 2]       (splits > 1)
+  uint16_t* out;               // bf16 bits [T, Hq, 128]   (splits == 1)
+  unsigned* err;
+  int B, Q, Hq, Hkv, S, splits;
+  int64_t num_blocks;
+  float logit_scale;           // sm_scale * k_scale * log2(e)
+  float v_scale;
+};
+
+// Runs `set_up` once per device (e.g. raising a kernel's dynamic shared-memory
+// limit), so that later launches, including ones inside a CUDA-graph capture,
+// make no attribute calls.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& set_up) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = set_up();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
+                           int splits, cudaStream_t stream);
+
+}  // namespace msa

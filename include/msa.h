@@ -1,0 +1,208 @@
+/*
+ * msa.h -- C ABI of the GB300 (sm_103a) block-sparse GQA decode library.
+ *
+ * One decode step of indexer-selected block-sparse attention over a paged fp8
+ * KV cache, as the vLLM MiniMax-M3 sparse attention pages and the
+ * TensorRT-LLM PR #17171 "Custom decode kernels for MinimaxM3" describe it:
+ *
+ *   msa_score          per-block causal max of scaled q.k over each KV head's
+ *                      query-head group                        (stage 1)
+ *   msa_topk           top-16 block selection                  (stage 2)
+ *   msa_sparse_decode  split-K attention over the selected pages (stage 3)
+ *   msa_combine        merge of the split-K partials            (stage 4)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are raw DEVICE pointers to memory the caller owns
+ *    and keeps alive until the work enqueued on `stream` has finished.  The
+ *    library allocates nothing and keeps no reference after returning.
+ *  - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns without waiting.  No call
+ *    synchronises the host except msa_get_error.
+ *  - Sizes: B requests, Q = decode_query_len query tokens per request,
+ *    T = B*Q query tokens ordered request-major (token i = b*Q + j),
+ *    Hq query heads and Hkv KV heads with Hq = 16 * Hkv (query head h belongs
+ *    to KV head g = h / 16), head size 128, page size 128 tokens, S = the
+ *    block_table row stride (max logical blocks per request), num_blocks =
+ *    physical pages in the cache.
+ *  - Causal offset: query token j of request b sits at position
+ *    pos = seq_lens[b] - Q + j and may see cache tokens 0..pos; its current
+ *    block is cur = pos / 128.  A token with pos < 0 is a padding row.
+ *  - Layouts (all contiguous, row-major):
+ *      q           bf16  [T, Hq, 128]
+ *      kv          fp8 e4m3 (OCP "fn") bytes [num_blocks, Hkv, 128, 256]:
+ *                  per page and KV head, 128 token rows of 256 bytes, K in
+ *                  bytes 0..127 and V in bytes 128..255 (the packed HND cache
+ *                  of MiniMaxM3SparseBackend.get_kv_cache_shape)
+ *      block_table int32 [B, S]; entry [b, n] = physical page of logical block n
+ *      seq_lens    int32 [B]
+ *      scores      fp32  [Hkv, T, S] (msa_score output)
+ *      topk        int32 [T, Hkv, 16], -1 = unused slot
+ *      out         bf16  [T, Hq, 128]
+ *  - Return value: MSA_OK, or an MSA_E* code when the call was rejected on
+ *    the host (nothing was enqueued) or a CUDA call failed.
+ *  - Bad indices found on the device (see MSA_ERR_*) never trap: the bad
+ *    entry is skipped and a bit is set in a per-device sticky error word that
+ *    msa_get_error reads.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so callers need no CUDA header to use this one. */
+typedef struct CUstream_st *msa_stream_t;
+
+/* ---- status codes ------------------------------------------------------- */
+#define MSA_OK 0
+#define MSA_EINVAL 1  /* bad size, null or misaligned pointer: rejected on host */
+#define MSA_ECUDA 3   /* a CUDA runtime call failed (no device, launch error)  */
+#define MSA_ENOSPC 4  /* workspace smaller than msa_workspace_bytes()          */
+
+/* ---- bits of the device error word (msa_get_error) ---------------------- */
+#define MSA_ERR_TOPK_RANGE 0x01u  /* top-k entry not -1 and outside [0, cur]          */
+#define MSA_ERR_TOPK_DUP 0x02u    /* a block listed twice for one (token, KV head)    */
+#define MSA_ERR_PAGE_RANGE 0x04u  /* block_table entry outside [0, num_blocks)        */
+#define MSA_ERR_SEQ_RANGE 0x08u   /* seq_lens[b] < 0 or ceil(seq_lens[b]/128) > S     */
+#define MSA_ERR_SCORE_NAN 0x10u   /* msa_topk read a NaN score (ranked as -inf)       */
+#define MSA_ERR_TIMEOUT 0x20u     /* a bounded wait for an async copy expired         */
+
+/* ---- fixed geometry ----------------------------------------------------- */
+#define MSA_HEAD_DIM 128
+#define MSA_PAGE_SIZE 128
+#define MSA_TOPK 16
+#define MSA_GROUP 16      /* query heads per KV head */
+#define MSA_MAX_QLEN 32
+
+/*
+ * msa_score -- stage 1, the block scorer.
+ *
+ * Defined by the scorer commit of TensorRT-LLM PR #17171 ("the same
+ * per-block causal max of Q.K", written in [head, token, block] order): for
+ * every KV head g, query token i and logical block n < S,
+ *
+ *   scores[g, i, n] = max over query heads h of group g and over tokens t of
+ *                     block n with 128*n + t <= pos(i) of
+ *                     sm_scale * k_scale * sum_d q[i,h,d] * K8[page(b,n),g,t,d]
+ *
+ * where K8 is the fp8 key as stored (the cache's K half).  Blocks n > cur(i)
+ * and every block of a padding row get -inf.  The whole [Hkv, T, S] buffer is
+ * written.  sm_scale > 0 and k_scale > 0 (both finite) are required.
+ * Numerics: fp8 keys are widened exactly; each query row is scaled by a power
+ * of two and rounded to fp16 (exact for the row's elements down to 2^-28 of
+ * its largest one), products accumulate in fp32.
+ * Errors: MSA_EINVAL for Q outside 1..32, Hq != 16*Hkv, S < 1, num_blocks < 1,
+ * num_blocks*Hkv*128 >= 2^31, null or non-16-byte-aligned q/kv, null
+ * block_table/seq_lens/scores.  Device: MSA_ERR_PAGE_RANGE (block scored
+ * -inf), MSA_ERR_SEQ_RANGE (request treated as empty).
+ */
+int msa_score(const void *q, const void *kv, const int32_t *block_table,
+              const int32_t *seq_lens, float *scores, int B, int Q, int Hq, int Hkv,
+              int S, int64_t num_blocks, float sm_scale, float k_scale,
+              msa_stream_t stream);
+
+/*
+ * msa_topk -- stage 2, the block selector.
+ *
+ * The selector of TensorRT-LLM PR #17171 reads the score buffer through
+ * arbitrary strides; the kept-block list follows the vLLM test file's
+ * _make_topk (ascending block ids, -1 padding).  For each (token i, KV head g)
+ * with pos(i) >= 0:
+ *   - if cur + 1 <= k every block 0..cur is kept;
+ *   - else block cur is kept together with the k-1 best of 0..cur-1 in the
+ *     order (score descending, block index ascending).
+ * Kept ids are written ascending to topk[i, g, 0..], the rest is -1.  Padding
+ * rows get all -1.  scores[g, i, n] is read at
+ * scores + g*stride_h + i*stride_t + n*stride_n (element strides, any sign);
+ * only n < cur is read.  The choice is exact (ties by index) for the given fp32
+ * values; -0.0 ranks equal to +0.0.
+ * Errors: MSA_EINVAL for k != 16, Q outside 1..32, Hkv < 1, S < 1, null or
+ * misaligned pointers.  Device: MSA_ERR_SEQ_RANGE (row written as padding),
+ * MSA_ERR_SCORE_NAN.
+ */
+int msa_topk(const float *scores, int64_t stride_h, int64_t stride_t, int64_t stride_n,
+             const int32_t *seq_lens, int32_t *topk, int B, int Q, int Hkv, int S, int k,
+             msa_stream_t stream);
+
+/*
+ * Bytes of workspace msa_sparse_decode needs for `num_splits` (0 if
+ * num_splits <= 1): fp32 partial outputs [num_splits, T, Hq, 128] followed by
+ * fp32 (m, l) pairs [num_splits, T, Hq, 2].  Returns 0 for invalid sizes.
+ */
+size_t msa_workspace_bytes(int B, int Q, int Hq, int num_splits);
+
+/*
+ * Split-K factor the library would pick for this shape on a GPU with
+ * `sm_count` SMs.  Depends on the shape only (never on seq_lens), so a step
+ * captured in a CUDA graph keeps a fixed launch shape.  Returns >= 1.
+ */
+int msa_choose_splits(int B, int Q, int Hkv, int sm_count);
+
+/*
+ * msa_sparse_decode -- stage 3 (+ stage 4 when split), the sparse attend.
+ *
+ * The operation of minimax_m3_sparse_attn_decode and msa_cutlass_sparse_decode
+ * on the vLLM pages: for each query row (i, h), g = h / 16, the key set is
+ * every token t of every block n listed in topk[i, g, :] (entries -1 skipped)
+ * with 128*n + t <= pos(i), and
+ *
+ *   out[i, h] = sum_t softmax_t(sm_scale * k_scale * q[i,h].K8_t) * v_scale * V8_t
+ *
+ * with no softcap, sink or output scale (o_scale = 1 on the vLLM page).  An
+ * empty key set or a padding row gives exactly 0 (the TensorRT-LLM
+ * flash-decoding commit zeroes padding rows instead of writing NaN).
+ * Entries may be in any order.  num_splits = 0 lets the library choose
+ * (msa_choose_splits); with an effective split count above 1 the partials go
+ * to `workspace` and msa_combine is enqueued on `stream` by this call, so
+ * `out` is complete when the stream reaches that point either way.
+ * Numerics: fp8 K/V widened exactly to fp16, q rows power-of-two scaled to
+ * fp16, probabilities rounded to fp16, fp32 accumulation and softmax, output
+ * rounded to bf16 (nearest even).
+ * Errors: as msa_score, plus null/misaligned topk or out, v_scale not finite,
+ * num_splits < 0 or > 16 (MSA_EINVAL), workspace_bytes too small (MSA_ENOSPC).
+ * Device: MSA_ERR_TOPK_RANGE / MSA_ERR_TOPK_DUP / MSA_ERR_PAGE_RANGE (entry
+ * skipped), MSA_ERR_SEQ_RANGE (request treated as empty).
+ */
+int msa_sparse_decode(const void *q, const void *kv, const int32_t *block_table,
+                      const int32_t *seq_lens, const int32_t *topk, void *workspace,
+                      size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv,
+                      int S, int64_t num_blocks, float sm_scale, float k_scale,
+                      float v_scale, int num_splits, msa_stream_t stream);
+
+/*
+ * msa_combine -- stage 4, merge of split-K partials ("fp32 split-K partials"
+ * in the TensorRT-LLM flash-decoding commit).  For row r of T*Hq rows, part s
+ * holds m_s (max logit in log2 units), l_s = sum 2^(z*log2(e) - m_s) and the
+ * unnormalised o_s = sum 2^(z*log2(e) - m_s) * V (V already times v_scale):
+ *
+ *   out[r] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s,
+ *
+ * parts with l_s = 0 ignored, and 0 when every part is empty.  `workspace`
+ * uses the layout msa_workspace_bytes describes.  num_splits in 1..16.
+ */
+int msa_combine(const void *workspace, void *out, int T, int Hq, int num_splits,
+                msa_stream_t stream);
+
+/*
+ * Read the current device's sticky error word (an OR of MSA_ERR_* bits set by
+ * any earlier call on any stream) into *flags, and reset it when `clear` is
+ * non-zero.  Synchronises the device first.  Returns MSA_OK or MSA_ECUDA.
+ */
+int msa_get_error(unsigned int *flags, int clear);
+
+/* Human-readable text for a status code. */
+const char *msa_strerror(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

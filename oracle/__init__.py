@@ -12,6 +12,7 @@ What each routine computes, and which page passage it follows, is stated in
 from __future__ import annotations
 
 import ctypes
+import fcntl
 import os
 import subprocess
 import threading
@@ -46,13 +47,19 @@ def build(force: bool = False) -> str:
     if override:
         return override
     os.makedirs(_OUT_DIR, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
-    if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fno-fast-math", "-Wall",
-                               "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _LIB_PATH)
+
+    def stale():
+        return (not os.path.exists(_LIB_PATH)
+                or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+
+    if force or stale():
+        with open(os.path.join(_OUT_DIR, ".lock"), "w") as lock:
+            fcntl.flock(lock, fcntl.LOCK_EX)
+            if force or stale():
+                tmp = _LIB_PATH + f".tmp{os.getpid()}"
+                subprocess.check_call(["gcc", "-std=c11", "-O2", "-fno-fast-math", "-Wall",
+                                       "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp, "-lm"])
+                os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
 
@@ -71,13 +78,15 @@ def _load():
             lib.orc_score.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i64, f64, f64, i32]
             lib.orc_score_units.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i64,
                                             f64, f64, i32]
+            lib.orc_score_blocks.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i64,
+                                             f64, f64, i32]
             lib.orc_topk.argtypes = [P, i64, i64, i64, P, P, i32, i32, i32, i32, i32]
             lib.orc_attend.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i64, i32, f64,
                                        f64, f64, i32]
             lib.orc_attend_rows.argtypes = [P, P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i64,
                                             i32, f64, f64, f64, i32]
             lib.orc_combine.argtypes = [P, P, P, i64, i32]
-            for name in ("orc_score", "orc_score_units", "orc_topk", "orc_attend",
+            for name in ("orc_score", "orc_score_units", "orc_score_blocks", "orc_topk", "orc_attend",
                          "orc_attend_rows", "orc_combine"):
                 getattr(lib, name).restype = i32
             _lib = lib
@@ -165,6 +174,18 @@ def score_units(p: Problem, units, nthreads: int = 0) -> np.ndarray:
                                  _ptr(out), _ptr(units), len(units), p.B, p.Q, p.Hq, p.Hkv, p.S,
                                  p.NB, p.sm_scale, p.k_scale, nthreads)
     _check(st, "score_units")
+    return out
+
+
+def score_blocks(p: Problem, triples, nthreads: int = 0) -> np.ndarray:
+    """Scores of listed (b, g, n) blocks for every token of request b; other
+    entries are NaN.  Returns the full [Hkv, T, S] array."""
+    triples = _c(np.asarray(triples, dtype=np.int64).reshape(-1, 3), np.int64)
+    out = np.full((p.Hkv, p.T, p.S), np.nan, dtype=np.float64)
+    st = _load().orc_score_blocks(_ptr(p.q), _ptr(p.kv), _ptr(p.block_table), _ptr(p.seq_lens),
+                                  _ptr(out), _ptr(triples), len(triples), p.B, p.Q, p.Hq, p.Hkv,
+                                  p.S, p.NB, p.sm_scale, p.k_scale, nthreads)
+    _check(st, "score_blocks")
     return out
 
 

@@ -605,6 +605,71 @@ int orc_score_units(const uint16_t *q, const uint8_t *kv, const int32_t *block_t
     return orc_parallel_for(orc_score_units_item, &c, n_units, nthreads);
 }
 
+/* Scores of listed blocks only: triples[3u..3u+2] = (b, g, n); writes
+ * scores[g, b*Q + j, n] for every token j of request b, by the same definition
+ * as orc_score.  Used for sampled checks at sizes where whole rows are slow. */
+typedef struct {
+    const orc_problem *p;
+    double *scores;
+    const int64_t *triples;
+} orc_score_blocks_ctx;
+
+static int orc_score_blocks_item(void *vctx, int64_t u)
+{
+    orc_score_blocks_ctx *c = (orc_score_blocks_ctx *)vctx;
+    const orc_problem *p = c->p;
+    int G = p->Hq / p->Hkv;
+    int b = (int)c->triples[3 * u], g = (int)c->triples[3 * u + 1];
+    int64_t n = c->triples[3 * u + 2];
+    for (int j = 0; j < p->Q; ++j) {
+        int i = b * p->Q + j;
+        int64_t pos = orc_pos(p, b, j);
+        double *slot = c->scores + ((int64_t)g * p->B * p->Q + i) * p->S + n;
+        *slot = -INFINITY;
+        if (pos < 0 || n > pos / ORC_PAGE)
+            continue;
+        int64_t page;
+        int st = orc_page(p, b, n, &page);
+        if (st != ORC_OK)
+            return st;
+        double best = -INFINITY;
+        for (int hh = 0; hh < G; ++hh) {
+            int h = g * G + hh;
+            for (int t = 0; t < ORC_PAGE; ++t) {
+                if (n * ORC_PAGE + t > pos)
+                    break;
+                double z = orc_logit(p, i, h, page, g, t);
+                if (isnan(z))
+                    return ORC_ENAN;
+                if (z > best)
+                    best = z;
+            }
+        }
+        *slot = best;
+    }
+    return ORC_OK;
+}
+
+int orc_score_blocks(const uint16_t *q, const uint8_t *kv, const int32_t *block_table,
+                     const int32_t *seq_lens, double *scores, const int64_t *triples,
+                     int64_t n_triples, int B, int Q, int Hq, int Hkv, int S, int64_t NB,
+                     double sm_scale, double k_scale, int nthreads)
+{
+    orc_problem p = {q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, NB, sm_scale, k_scale, 1.0};
+    int st = orc_check_problem(&p);
+    if (st != ORC_OK)
+        return st;
+    if (!scores || !triples || n_triples < 0)
+        return ORC_EINVAL;
+    for (int64_t u = 0; u < n_triples; ++u) {
+        const int64_t *t = triples + 3 * u;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= Hkv || t[2] < 0 || t[2] >= S)
+            return ORC_EINVAL;
+    }
+    orc_score_blocks_ctx c = {&p, scores, triples};
+    return orc_parallel_for(orc_score_blocks_item, &c, n_triples, nthreads);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Split-softmax merge                                                       */
 /* ------------------------------------------------------------------------ */

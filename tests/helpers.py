@@ -88,3 +88,42 @@ def dense_reference(inp, topk=None):
                     p = torch.softmax(masked, dim=-1)
                     out[i, g * G:(g + 1) * G] = p @ V
     return out, scores
+
+
+# Tolerances of the decode step (fp32 block scores; bf16 outputs).
+SCORE_REL = 1e-3        # |gpu - ref| <= SCORE_REL * max(1, |ref|) on finite scores
+OUT_MAX_ABS = 2e-2      # bf16 outputs vs the fp64 oracle, max over all elements
+OUT_MEAN_ABS = 2e-3     # ... and mean over all elements
+
+
+def assert_scores_close(gpu: np.ndarray, ref: np.ndarray, mask: np.ndarray | None = None):
+    """Scores: -inf exactly where the oracle has -inf, relative 1e-3 elsewhere."""
+    if mask is None:
+        mask = np.ones(ref.shape, dtype=bool)
+    g, r = gpu[mask], ref[mask]
+    inf = np.isneginf(r)
+    assert np.array_equal(np.isneginf(g), inf), "-inf pattern differs"
+    fin = ~inf
+    assert np.all(np.isfinite(g[fin]))
+    err = np.abs(g[fin] - r[fin]) / np.maximum(1.0, np.abs(r[fin]))
+    assert err.size == 0 or err.max() <= SCORE_REL, f"score rel err {err.max():.3e}"
+
+
+def assert_out_close(gpu: np.ndarray, ref: np.ndarray, zero_rows: np.ndarray | None = None):
+    """bf16 outputs: max-abs <= 2e-2 and mean-abs <= 2e-3; padding rows exactly 0."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    d = np.abs(gpu - ref)
+    assert np.all(np.isfinite(gpu)), "non-finite output"
+    assert d.max() <= OUT_MAX_ABS, f"max abs err {d.max():.3e}"
+    assert d.mean() <= OUT_MEAN_ABS, f"mean abs err {d.mean():.3e}"
+    if zero_rows is not None and zero_rows.any():
+        assert np.all(gpu[zero_rows] == 0.0), "padding rows must be exactly zero"
+
+
+def padding_rows(seq_lens, qlen: int) -> np.ndarray:
+    """[T] bool: query tokens with pos = seq_len - qlen + j < 0."""
+    rows = []
+    for L in seq_lens:
+        for j in range(qlen):
+            rows.append(L - qlen + j < 0)
+    return np.array(rows, dtype=bool)

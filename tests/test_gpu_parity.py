@@ -1,0 +1,199 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the same
+seeded inputs.  Bar: top-k bit-exact given identical scores; scores within
+relative 1e-3; bf16 outputs within max-abs 2e-2 and mean-abs 2e-3, padding rows
+exactly zero."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_gqa_score_gb300 as msa
+import oracle
+from block_sparse_gqa_score_gb300 import workloads as wl
+from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, to_problem)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    msa.get_error(clear=True)
+    yield
+
+
+def _np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64) if t.dtype == torch.bfloat16 \
+        else t.detach().cpu().numpy()
+
+
+# The vLLM interleaved-cache test's shapes: seq_lens [257, 513] x pairs with
+# qlen in {1, 2, 3, 4, 8}, tp1 (64/4) and tp4 (16/1) head geometries, then the
+# ragged update [129, 385]; plus short, padding and long rows of our own.
+SMALL_CASES = [
+    ([257, 513] * 2, 1, 64, 4),
+    ([257, 513] * 2, 2, 64, 4),
+    ([257, 513] * 2, 3, 64, 4),
+    ([257, 513] * 2, 4, 16, 1),
+    ([257, 513] * 2, 8, 64, 4),
+    ([129, 385] * 2, 4, 64, 4),
+    ([0, 2, 3, 130, 2048, 2049], 4, 16, 1),       # padding rows, page boundaries
+    ([3000, 5000, 4100], 1, 32, 2),
+    ([2500, 700], 32, 16, 1),                     # qlen at its upper bound
+    ([6000, 1], 5, 64, 4),
+]
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", SMALL_CASES)
+def test_score_matches_oracle(seq_lens, Q, Hq, Hkv):
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=101, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax", min_stride=3)
+    gpu = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale)
+    ref = oracle.score(to_problem(inp, oracle))
+    assert_scores_close(_np(gpu).astype(np.float64), ref)
+    assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", SMALL_CASES)
+def test_topk_bit_exact_given_gpu_scores(seq_lens, Q, Hq, Hkv):
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=102, device=DEV, min_stride=3)
+    scores = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale)
+    got = msa.topk(scores, inp.seq_lens, Q)
+    want = oracle.topk(_np(scores).astype(np.float64), np.array(seq_lens, dtype=np.int32), Q)
+    assert np.array_equal(_np(got), want)
+
+
+@pytest.mark.parametrize("S,cur_lo", [(40, 17), (300, 200), (3000, 2500)])
+def test_topk_ties_and_strides(S, cur_lo):
+    """Integer-valued scores force ties; the buffer is stored [Hkv, S, T] and
+    read through its transposed view (arbitrary strides); S = 3000 exercises
+    rows longer than the selector's shared-memory cache."""
+    g = torch.Generator().manual_seed(S)
+    B, Q, Hkv = 3, 4, 2
+    seq_lens = torch.randint(cur_lo * 128, S * 128 - 4, (B,), generator=g).to(torch.int32)
+    phys = torch.randint(-4, 5, (Hkv, S, B * Q), generator=g).float()
+    phys[0, 5, :] = -0.0
+    phys[1, 7, :] = 0.0
+    scores = phys.to(DEV).transpose(1, 2)           # [Hkv, T, S] view
+    got = msa.topk(scores, seq_lens.to(DEV), Q)
+    want = oracle.topk(phys.double().numpy().transpose(0, 2, 1), seq_lens.numpy(), Q)
+    assert np.array_equal(_np(got), want)
+
+
+ATTEND_CASES = SMALL_CASES + [([20000, 9000, 40000], 4, 64, 4), ([70000], 2, 16, 1)]
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", ATTEND_CASES)
+@pytest.mark.parametrize("splits", [1, 3])
+def test_attend_matches_oracle(seq_lens, Q, Hq, Hkv, splits):
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=103, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    gen = torch.Generator().manual_seed(7)
+    topk = wl.draw_topk_given(seq_lens, Q, Hkv, gen)
+    out = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk.to(DEV), Q,
+                            inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=splits)
+    ref = oracle.attend(to_problem(inp, oracle), topk.numpy())
+    assert_out_close(_np(out), ref, padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
+
+
+def test_attend_pages_all_visible_topk_graph_replay():
+    """The vLLM test's flow: all-visible top-k for [257, 513], then ragged
+    [129, 385] written in place, captured in a CUDA graph and replayed after
+    the lengths change back."""
+    Q, Hq, Hkv = 4, 64, 4
+    lens_a, lens_b = [257, 513] * 8, [129, 385] * 8
+    inp = wl.make_custom(lens_a, Q, Hq, Hkv, seed=104, device=DEV, kv_std=0.25)
+    topk = wl.all_visible_topk(lens_a, Q, Hkv).to(DEV)
+    out = torch.empty_like(inp.q)
+    ws = torch.empty(msa.workspace_bytes(16, Q, Hq, 2) or 1, dtype=torch.uint8, device=DEV)
+
+    def run():
+        msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, Q, inp.sm_scale,
+                          out=out, num_splits=2, workspace=ws)
+
+    run()
+    assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), topk.cpu().numpy()))
+    inp.seq_lens.copy_(torch.tensor(lens_b, dtype=torch.int32))
+    topk.copy_(wl.all_visible_topk(lens_b, Q, Hkv))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()                               # warm-up on the capture stream
+        with torch.cuda.graph(graph, stream=s):
+            run()
+    torch.cuda.synchronize()
+    inp.seq_lens.copy_(torch.tensor(lens_a, dtype=torch.int32))
+    topk.copy_(wl.all_visible_topk(lens_a, Q, Hkv))
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    inp.seq_lens_list = lens_a
+    assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), topk.cpu().numpy()))
+
+
+def test_split_counts_agree():
+    inp = wl.make_custom([30000, 12000, 50000, 999], 4, 64, 4, seed=105, device=DEV)
+    topk = wl.draw_topk_given(inp.seq_lens_list, 4, 4, torch.Generator().manual_seed(1)).to(DEV)
+    outs = [msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, 4,
+                              inp.sm_scale, num_splits=s).float() for s in (1, 2, 5, 16)]
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 4e-3
+
+
+def test_combine_matches_oracle():
+    T, Hq, splits = 6, 32, 5
+    g = torch.Generator().manual_seed(3)
+    rows = T * Hq
+    o = torch.randn((splits, rows, 128), generator=g, dtype=torch.float64)
+    m = torch.randn((splits, rows), generator=g, dtype=torch.float64) * 4
+    l = torch.rand((splits, rows), generator=g, dtype=torch.float64) * 10
+    l[1, :7] = 0.0                          # empty parts
+    m[1, :7] = -float("inf")
+    l[:, 9] = 0.0                           # a row with every part empty
+    m[:, 9] = -float("inf")
+    ml = torch.stack([m, l], dim=-1)
+    ws = torch.cat([o.float().reshape(-1), ml.float().reshape(-1)]).to(DEV)
+    got = msa.combine(ws, T, Hq, splits)
+    want = oracle.combine(o.float().double().numpy(), ml.float().double().numpy())
+    d = np.abs(_np(got).reshape(rows, 128) - want)
+    assert d.max() <= 2e-2 and np.all(_np(got).reshape(rows, 128)[9] == 0)
+
+
+def test_decode_step_tiny_workload_end_to_end():
+    inp = wl.make_inputs("tiny_b2_q1_h16kv1_2k3k", device=DEV)
+    scores, topk, out = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
+                                        inp.sm_scale, inp.k_scale, inp.v_scale)
+    p = to_problem(inp, oracle)
+    s_ref, t_ref, o_ref = oracle.decode_step(p)
+    assert_scores_close(_np(scores).astype(np.float64), s_ref)
+    assert np.array_equal(_np(topk), t_ref)
+    assert_out_close(_np(out), o_ref)
+    assert msa.get_error() == 0
+
+
+def test_bad_indices_are_flagged_and_skipped():
+    seq_lens = [1000, 600]
+    inp = wl.make_custom(seq_lens, 1, 16, 1, seed=106, device=DEV)
+    good = wl.all_visible_topk(seq_lens, 1, 1)
+    bad = good.clone()
+    bad[0, 0, 8] = 9          # cur is 7: out of range
+    bad[1, 0, 5] = 2          # duplicate of slot 2
+    out = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bad.to(DEV), 1,
+                            inp.sm_scale)
+    flags = msa.get_error()
+    assert flags & msa._native.ERR_TOPK_RANGE and flags & msa._native.ERR_TOPK_DUP
+    assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), good.numpy()))
+    bt = inp.block_table.clone()
+    bt[1, 1] = inp.num_blocks + 5
+    msa.sparse_decode(inp.q, inp.kv, bt, inp.seq_lens, good.to(DEV), 1, inp.sm_scale)
+    assert msa.get_error() & msa._native.ERR_PAGE_RANGE
+    msa.score(inp.q, inp.kv, bt, inp.seq_lens, 1, inp.sm_scale)
+    assert msa.get_error() & msa._native.ERR_PAGE_RANGE
+    long = inp.seq_lens.clone()
+    long[0] = inp.stride * 128 + 1
+    msa.topk(torch.zeros((1, 2, inp.stride), device=DEV), long, 1)
+    assert msa.get_error() & msa._native.ERR_SEQ_RANGE

@@ -41,9 +41,9 @@ MUTANTS = {
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
     mut = tmp_path / "mutant.c"
-    mut.write_text(src.replace(old, new))
+    mut.write_text(src.replace(old, new))     # every copy of the site gets the same mistake
     lib = tmp_path / "libmutant.so"
     subprocess.check_call(["gcc", "-std=c11", "-O2", "-shared", "-fPIC", "-pthread", str(mut),
                            "-o", str(lib), "-lm"])

@@ -347,3 +347,14 @@ def test_decode_step_on_tiny_workload_is_consistent():
     assert worst_kept >= best_dropped
     ref, _ = dense_reference(inp, torch.from_numpy(t))
     np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_score_blocks_matches_full_scores():
+    inp = wl.make_custom([3000, 1500], 3, 32, 2, seed=37)
+    p = to_problem(inp, oracle)
+    full = oracle.score(p)
+    triples = [(0, 1, 23), (1, 0, 0), (1, 1, 11), (0, 0, 5), (1, 0, 20)]
+    part = oracle.score_blocks(p, triples)
+    for b, g, n in triples:
+        rows = slice(b * 3, b * 3 + 3)
+        assert np.array_equal(part[g, rows, n], full[g, rows, n])
