@@ -409,8 +409,9 @@ def run_ours(args, rank, world, local):
             graphs.append((capture(chunk, 0), full))
         if rem:
             graphs.append((capture(rem, 0), 1))
-        for (g, _), _n in graphs:      # one untimed pass: graph upload
-            g.replay()
+        with torch.cuda.stream(stream):
+            for (g, _), _n in graphs:  # one untimed pass: graph upload
+                g.replay()
         torch.cuda.synchronize(dev)
     except Exception as e:  # pragma: no cover - depends on the torch build
         mode = f"eager ({type(e).__name__})"
@@ -425,9 +426,10 @@ def run_ours(args, rank, world, local):
     clocks.mark_start()
     start.record(stream)
     if graphs:
-        for (g, _evs), reps in graphs:
-            for _ in range(reps):
-                g.replay()
+        with torch.cuda.stream(stream):          # replays launch on the current stream
+            for (g, _evs), reps in graphs:
+                for _ in range(reps):
+                    g.replay()
     else:
         with torch.cuda.stream(stream):
             for k in range(args.steps):

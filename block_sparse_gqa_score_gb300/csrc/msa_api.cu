@@ -84,7 +84,11 @@ int check_common(const void* q, const void* kv, const int32_t* block_table,
 
 // 2-D view of the cache as [num_blocks * Hkv * 128 rows, 256 bytes], read in
 // 128 x 128-byte boxes (one K or V half of a page-head) with 128B swizzling.
-int encode_kv_map(const void* kv, int Hkv, int64_t num_blocks, CUtensorMap* map) {
+// `l2_256` promotes L2 fills to 256 bytes (both halves of a token row, for the
+// attend); the scorer reads K halves only and keeps 128-byte fills so the V
+// halves are not dragged in from DRAM.
+int encode_kv_map(const void* kv, int Hkv, int64_t num_blocks, CUtensorMap* map,
+                  bool l2_256 = true) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2),
                         static_cast<cuuint64_t>(num_blocks) * Hkv * MSA_PAGE_SIZE};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2)};
@@ -92,7 +96,9 @@ int encode_kv_map(const void* kv, int Hkv, int64_t num_blocks, CUtensorMap* map)
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        l2_256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                               : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MSA_OK : MSA_EINVAL;
 }
 
@@ -142,7 +148,7 @@ int msa_score(const void* q, const void* kv, const int32_t* block_table, const i
   DeviceState* dev;
   if ((st = device_state(&dev)) != MSA_OK) return st;
   CUtensorMap map;
-  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map, /*l2_256=*/false)) != MSA_OK) return st;
   msa::ScoreParams p{};
   p.q = static_cast<const uint16_t*>(q);
   p.block_table = block_table;
