@@ -269,3 +269,67 @@ int msa_get_error(unsigned int* flags, int clear) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of msa_sparse_decode.
+//
+// Some callers cannot allocate device memory at all: a plugin or operator
+// interface that hands the library only the step's input and output buffers
+// and gives it no workspace, or a runtime that forbids cudaMalloc on its hot
+// path because an allocation can block on the whole device or fail under
+// memory pressure.  For them the split-K partials live in one fixed scratch
+// array compiled into the library.  Every GPU that loads the library holds
+// this array until the process exits, so its size is kept modest.
+
+static __device__ __align__(256) unsigned char msa_static_scratch[MSA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_mutex;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's name
+// is only a host-side stand-in in host code, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSA_ECUDA;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, msa_static_scratch) != cudaSuccess || !ptr) return MSA_ECUDA;
+    g_static_scratch_ptr[dev] = ptr;
+  }
+  *out = g_static_scratch_ptr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" int msa_sparse_decode_static(const void* q, const void* kv,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        const int32_t* topk, void* out, int B, int Q, int Hq,
+                                        int Hkv, int S, int64_t num_blocks, float sm_scale,
+                                        float k_scale, float v_scale, int num_splits,
+                                        msa_stream_t stream) {
+  int splits = num_splits;
+  if (splits == 0 && B >= 1 && Q >= 1 && Hkv >= 1) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MSA_ECUDA;
+    splits = msa_choose_splits(B, Q, Hkv, sms);
+  }
+  const size_t need = msa_workspace_bytes(B, Q, Hq, splits);
+  if (need > MSA_STATIC_SCRATCH_BYTES) return MSA_ENOSPC;
+  void* scratch = nullptr;
+  if (need > 0) {
+    const int st = static_scratch_address(&scratch);
+    if (st != MSA_OK) return st;
+  }
+  // Same validation and kernels as msa_sparse_decode; the partials go to the
+  // static array instead of a caller-provided workspace.
+  return msa_sparse_decode(q, kv, block_table, seq_lens, topk, scratch,
+                           need > 0 ? static_cast<size_t>(MSA_STATIC_SCRATCH_BYTES) : 0, out, B,
+                           Q, Hq, Hkv, S, num_blocks, sm_scale, k_scale, v_scale, splits, stream);
+}

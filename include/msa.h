@@ -189,6 +189,37 @@ int msa_combine(const void *workspace, void *out, int T, int Hq, int num_splits,
                 msa_stream_t stream);
 
 /*
+ * msa_sparse_decode_static -- msa_sparse_decode for callers that cannot
+ * allocate device memory.  The paper has no counterpart for it; it exists for
+ * callers that only hold the step's inputs and outputs: a plugin or operator
+ * interface that gives the library no workspace, or a runtime that forbids
+ * cudaMalloc on its hot path (an allocation can block on the whole device or
+ * fail under memory pressure).
+ *
+ * Same arguments and result as msa_sparse_decode without the workspace pair.
+ * The split-K partials go to one scratch array compiled into the library:
+ * MSA_STATIC_SCRATCH_BYTES (4 MiB) of device memory that every GPU loading
+ * the library holds until the process exits.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *  - A shape whose partials need more than MSA_STATIC_SCRATCH_BYTES
+ *    (msa_workspace_bytes(B, Q, Hq, splits) > MSA_STATIC_SCRATCH_BYTES) is
+ *    rejected with MSA_ENOSPC before anything is enqueued; pass a smaller
+ *    num_splits (1 needs no scratch) or use msa_sparse_decode.
+ *  - The first call on a device that needs the scratch looks up the array's
+ *    device address (cudaGetSymbolAddress) with that device current; make
+ *    that first call before any stream capture.
+ *  - All calls share the one array, and it keeps the last call's contents.
+ *    Nothing in it has to start at zero (each call writes every partial it
+ *    reads back), but calls whose work overlaps on the GPU, e.g. on two
+ *    streams at once, race on the array and give wrong results.
+ */
+#define MSA_STATIC_SCRATCH_BYTES (4u << 20)
+int msa_sparse_decode_static(const void *q, const void *kv, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *topk, void *out, int B,
+                             int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                             float k_scale, float v_scale, int num_splits, msa_stream_t stream);
+
+/*
  * Read the current device's sticky error word (an OR of MSA_ERR_* bits set by
  * any earlier call on any stream) into *flags, and reset it when `clear` is
  * non-zero.  Synchronises the device first.  Returns MSA_OK or MSA_ECUDA.
