@@ -42,6 +42,8 @@ SMALL_CASES = [
     ([3000, 5000, 4100], 1, 32, 2),
     ([2500, 700], 32, 16, 1),                     # qlen at its upper bound
     ([6000, 1], 5, 64, 4),
+    ([9000, 300], 16, 32, 2),                     # 256 query rows: one full MMA N
+    ([5000, 17, 4500], 17, 16, 1),                # 272 rows: two MMA units of 9 + 8 tokens
 ]
 
 
