@@ -42,9 +42,13 @@ struct AttendSmemTail {
   int pos;
 };
 
+// fp16 query fragments shared by the compute warps: [k-step][lane] uint4
+constexpr int kQfragBytes = 8 * 32 * 16;
+constexpr int kTailBytes = static_cast<int>((sizeof(AttendSmemTail) + 15) / 16 * 16);
+
 template <int NST>
 constexpr int attend_smem_bytes() {
-  return NST * kStageBytes + static_cast<int>(sizeof(AttendSmemTail)) + 1024;
+  return NST * kStageBytes + kTailBytes + kQfragBytes + 1024;
 }
 
 // Returns the PRMT selector that gathers byte r of x and byte r of y into the
@@ -60,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   AttendSmemTail* tail = reinterpret_cast<AttendSmemTail*>(smem + NST * kStageBytes);
+  uint4* qfrag = reinterpret_cast<uint4*>(smem + NST * kStageBytes + kTailBytes);  // [8][32]
 
   const int i = blockIdx.x;      // query token
   const int g = blockIdx.y;      // KV head
@@ -149,11 +154,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ---- compute warps ---------------------------------------------------------
   const int gr = lane >> 2, c = lane & 3;
   const int key0 = warp * 32;
-  uint32_t qa[8][4];
-  float zs0, zs1;
-  load_query_fragments(p.q + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim, lane,
-                       p.logit_scale, qa, zs0, zs1);
+  float zs0, zs1;  // logit scales (log2 units) of rows gr / gr+8, times their power-of-two factors
+  {
+    // every warp prepares the fp16 query fragments; warp w stores k-steps 2w, 2w+1
+    uint32_t qa[8][4];
+    load_query_fragments(p.q + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim, lane,
+                         p.logit_scale, qa, zs0, zs1);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      if ((ks >> 1) == warp)
+        qfrag[ks * 32 + lane] = make_uint4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+  named_barrier(1, kComputeWarps * 32);  // no wait precedes it: every compute warp arrives
 
+  // m0/m1: the reference maximum used for rows gr / gr+8 (lazily raised: it
+  // only moves when a page's maximum exceeds it by more than kLazy, so the
+  // probabilities stay <= 2^kLazy, well inside fp16).
+  constexpr float kLazy = 8.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float o[16][4];
 #pragma unroll
@@ -174,19 +191,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint8_t* kt = smem + s * kStageBytes;
     const uint8_t* vt = kt + kHalfTile;
     const int lim = pos - tail->blocks[t] * kPage;  // keys <= lim are visible
+    const bool whole = lim >= kPage - 1;            // same for the whole CTA
 
+    // S = Q K^T (fp16 MMA; fp8 keys widened in registers)
     float acc[4][4];
-    qk_32keys(kt, key0, lane, qa, acc);
-
-    // logits in log2 units, causal mask inside the current block
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[tt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint4 qv = qfrag[ks * 32 + lane];
+      const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        const int row = key0 + 8 * tt + gr;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + sw128(row, ks) + 4 * c);
+        mma_f16(acc[tt], qa, e4m3x2_to_f16x2(w & 0xFFFF), e4m3x2_to_f16x2(w >> 16));
+      }
+    }
+    if (!whole) {
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        const int key = key0 + 8 * tt + 2 * c;
+        if (key > lim) acc[tt][0] = acc[tt][2] = -INFINITY;
+        if (key + 1 > lim) acc[tt][1] = acc[tt][3] = -INFINITY;
+      }
+    }
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int tt = 0; tt < 4; ++tt) {
-      const int key = key0 + 8 * tt + 2 * c;
-      acc[tt][0] = (key <= lim) ? acc[tt][0] * zs0 : -INFINITY;
-      acc[tt][1] = (key + 1 <= lim) ? acc[tt][1] * zs0 : -INFINITY;
-      acc[tt][2] = (key <= lim) ? acc[tt][2] * zs1 : -INFINITY;
-      acc[tt][3] = (key + 1 <= lim) ? acc[tt][3] * zs1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(acc[tt][0], acc[tt][1]));
       mx1 = fmaxf(mx1, fmaxf(acc[tt][2], acc[tt][3]));
     }
@@ -194,40 +228,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    // rescale factors; a row with no visible key so far keeps m = -inf
-    const float al0 = (mn0 == -INFINITY) ? 1.f : ex2(m0 - mn0);
-    const float al1 = (mn1 == -INFINITY) ? 1.f : ex2(m1 - mn1);
-    const float sub0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float sub1 = (mn1 == -INFINITY) ? 0.f : mn1;
-
+    const float mz0 = mx0 * zs0, mz1 = mx1 * zs1;   // page maxima in log2 units
+    const bool r0 = mz0 > m0 + kLazy, r1 = mz1 > m1 + kLazy;
+    if (__any_sync(0xffffffffu, r0 || r1)) {
+      const float al0 = r0 ? ex2(m0 - mz0) : 1.f;  // ex2(-inf) = 0 on the first raise
+      const float al1 = r1 ? ex2(m1 - mz1) : 1.f;
+      if (r0) m0 = mz0;
+      if (r1) m1 = mz1;
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int dt = 0; dt < 16; ++dt) {
+        o[dt][0] *= al0;
+        o[dt][1] *= al0;
+        o[dt][2] *= al1;
+        o[dt][3] *= al1;
+      }
+    }
+    // p = 2^(acc*zs - m); a row with no visible key yet has m = -inf and only
+    // -inf logits, which give 0
+    const float nm0 = (m0 == -INFINITY) ? 0.f : -m0;
+    const float nm1 = (m1 == -INFINITY) ? 0.f : -m1;
     uint32_t pa[2][4];
-    float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int tt = 0; tt < 4; ++tt) {
-      const float p0 = ex2(acc[tt][0] - sub0), p1 = ex2(acc[tt][1] - sub0);
-      const float p2 = ex2(acc[tt][2] - sub1), p3 = ex2(acc[tt][3] - sub1);
-      rs0 += p0 + p1;
-      rs1 += p2 + p3;
+      const float p0 = ex2(fmaf(acc[tt][0], zs0, nm0)), p1 = ex2(fmaf(acc[tt][1], zs0, nm0));
+      const float p2 = ex2(fmaf(acc[tt][2], zs1, nm1)), p3 = ex2(fmaf(acc[tt][3], zs1, nm1));
+      l0 += p0 + p1;
+      l1 += p2 + p3;
       // C fragments of key tiles (2k, 2k+1) form the A fragment of PV k-step k
       pa[tt >> 1][(tt & 1) * 2 + 0] = pack_f16x2(p0, p1);
       pa[tt >> 1][(tt & 1) * 2 + 1] = pack_f16x2(p2, p3);
     }
-    l0 = l0 * al0 + rs0;
-    l1 = l1 * al1 + rs1;
-    m0 = mn0;
-    m1 = mn1;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      o[dt][0] *= al0;
-      o[dt][1] *= al0;
-      o[dt][2] *= al1;
-      o[dt][3] *= al1;
-    }
 
-    // O += P V.  Logical d-column n of d-tile 4*q4 + r is physical
+    // O += P V (fp16 MMA).  Logical d-column n of d-tile 4*q4 + r is physical
     // d = 4*(n + 8*q4) + r, so each lane's 4-byte load of one V row covers
     // four d-tiles; rows 2c, 2c+1, 2c+8, 2c+9 of the k-step give the B pairs.
+    // On the current block's page, rows past the causal limit are zeroed so
+    // that whatever bytes they hold cannot reach the output.
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const int rb = key0 + 16 * kk + 2 * c;
@@ -235,10 +273,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int q4 = 0; q4 < 4; ++q4) {
         const int chunk = (gr >> 2) + 2 * q4;
         const int word = 4 * (gr & 3);
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb, chunk) + word);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 1, chunk) + word);
-        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 8, chunk) + word);
-        const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 9, chunk) + word);
+        uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb, chunk) + word);
+        uint32_t w1 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 1, chunk) + word);
+        uint32_t w2 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 8, chunk) + word);
+        uint32_t w3 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 9, chunk) + word);
+        if (!whole) {
+          if (rb > lim) w0 = 0u;
+          if (rb + 1 > lim) w1 = 0u;
+          if (rb + 8 > lim) w2 = 0u;
+          if (rb + 9 > lim) w3 = 0u;
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const uint32_t b0 = e4m3x2_to_f16x2(pair_bytes(w0, w1, r));

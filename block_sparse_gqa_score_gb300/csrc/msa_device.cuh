@@ -174,6 +174,89 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// m16n8k32 tensor-core MMA, fp8 e4m3 inputs, fp32 accumulate (in place).
+// A (16 x 32, row): a0/a2 = row lane/4, k 4(lane%4)..+3 and 16 + that; a1/a3
+// the same for row lane/4 + 8.  B (32 x 8, col): b0/b1 = k 4(lane%4)..+3 and
+// 16 + that, column lane/4.
+__device__ __forceinline__ void mma_e4m3_k32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four floats -> four e4m3 bytes (x0 in the low byte).
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float x0, float x1, float x2, float x3) {
+  return f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
+}
+
+// Exact split of four floats (each with at most 8 significant bits and a
+// magnitude below 2^8) into fp8 e4m3 hi + lo words with hi + lo == x for
+// every element whose magnitude is at least 2^-2.
+__device__ __forceinline__ void split_e4m3x4(const float (&x)[4], uint32_t& hi, uint32_t& lo) {
+  const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
+  uint32_t w01 = e4m3x2_to_f16x2(h01), w23 = e4m3x2_to_f16x2(h23);
+  const __half2 f01 = *reinterpret_cast<const __half2*>(&w01);
+  const __half2 f23 = *reinterpret_cast<const __half2*>(&w23);
+  hi = h01 | (h23 << 16);
+  lo = f32x4_to_e4m3x4(x[0] - __low2float(f01), x[1] - __high2float(f01),
+                       x[2] - __low2float(f23), x[3] - __high2float(f23));
+}
+
+// Query fragments for the fp8 QK^T MMA (m16n8k32): the 16 query heads of one
+// (token, KV head), scaled by a per-token power of two 2^-e so that the
+// largest element lies in [2^7, 2^8), then split exactly into e4m3 hi + lo.
+// Lane (gr = lane/4, c = lane%4) gets, for k-step ks (d = 32ks .. 32ks+31):
+//   hi/lo[0] = row gr,   d 32ks + 4c .. +3      hi/lo[2] = row gr,   d +16
+//   hi/lo[1] = row gr+8, d 32ks + 4c .. +3      hi/lo[3] = row gr+8, d +16
+// Only k-step `ks_only` (0..3) is split and returned; the exponent e always
+// comes from the whole token.  `mul` receives scale * 2^e.
+__device__ __forceinline__ void load_query_fragments_e4m3(const uint16_t* __restrict__ q_rows,
+                                                          int lane, float scale, int ks_only,
+                                                          uint32_t (&hi)[4], uint32_t (&lo)[4],
+                                                          float& mul) {
+  const int gr = lane >> 2, c = lane & 3;
+  uint2 raw[4][4];  // [ks][fragment register]
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+      const int row = gr + 8 * (f & 1), d = 32 * ks + 16 * (f >> 1) + 4 * c;
+      raw[ks][f] = __ldg(reinterpret_cast<const uint2*>(q_rows + row * kHeadDim + d));
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].x & 0xFFFF)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].x >> 16)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].y & 0xFFFF)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].y >> 16)));
+    }
+  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+  const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  int e = (biased == 0 || biased == 0xFF) ? 0 : biased - 127 - 7;
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  const float sd = exp2i(-e);
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    if (ks != ks_only) continue;
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+      const float x[4] = {bf16_bits_to_f32(raw[ks][f].x & 0xFFFF) * sd,
+                          bf16_bits_to_f32(raw[ks][f].x >> 16) * sd,
+                          bf16_bits_to_f32(raw[ks][f].y & 0xFFFF) * sd,
+                          bf16_bits_to_f32(raw[ks][f].y >> 16) * sd};
+      split_e4m3x4(x, hi[f], lo[f]);
+    }
+  }
+  mul = scale * exp2i(e);
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -8,11 +8,13 @@
 // scorer's [head, token, block] buffer through a transposed view.
 //
 // Design: one warp per row.  Scores become order-preserving 32-bit keys
-// (larger float -> larger key, -0 folded onto +0).  A most-significant-digit
-// radix select (8 passes of 4 bits, shared-memory histograms) finds the exact
-// 15th-largest key tau and how many keys equal to tau are still needed; a
-// final ordered sweep keeps every key > tau and the lowest-index keys == tau.
-// Rows of up to kCache candidates are staged once in shared memory.
+// (larger float -> larger key, -0 folded onto +0).  The 15th-largest key tau
+// is found by a bitwise binary search from the most significant bit: for each
+// bit, count (one compare per key, one warp-wide redux add) the keys at or
+// above the candidate prefix, and keep the bit when at least 15 are.  Keys
+// > tau are all kept and the lowest-index keys == tau fill the rest, in one
+// ordered sweep.  Rows of up to 512 candidates live in registers (16 per
+// lane), rows up to kCache in shared memory, longer rows are re-read.
 #include "msa_device.cuh"
 #include "msa_launch.h"
 
@@ -22,6 +24,8 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kCache = 2048;  // candidates cached per warp (8 KiB)
+constexpr int kRegKeys = 16;  // candidates per lane held in registers
+constexpr int kSel = kTopK - 1;
 
 __device__ __forceinline__ uint32_t order_key(float x, bool& nan) {
   uint32_t u = __float_as_uint(x);
@@ -33,9 +37,33 @@ __device__ __forceinline__ uint32_t order_key(float x, bool& nan) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Bitwise search for the 15th-largest of a row's keys held NK per lane in
+// registers (lane + 32 e); also leaves the keys in `keys` for the final sweep.
+template <int NK, typename LoadKey>
+__device__ __forceinline__ uint32_t tau_in_registers(LoadKey& load_key, uint32_t* keys, int cur,
+                                                     int lane) {
+  uint32_t kr[NK];
+#pragma unroll
+  for (int e = 0; e < NK; ++e) {
+    const int n = lane + 32 * e;
+    kr[e] = (n < cur) ? load_key(n) : 0u;  // 0 ranks below every real key
+  }
+  uint32_t tau = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = tau | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < NK; ++e) cnt += (kr[e] >= cand) ? 1 : 0;
+    if (__reduce_add_sync(0xffffffffu, cnt) >= kSel) tau = cand;
+  }
+#pragma unroll
+  for (int e = 0; e < NK; ++e)
+    if (lane + 32 * e < cur) keys[lane + 32 * e] = kr[e];
+  return tau;
+}
+
 __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
   __shared__ uint32_t s_keys[kWarps][kCache];
-  __shared__ int s_hist[kWarps][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int T = p.B * p.Q;
@@ -59,43 +87,33 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
   }
 
   const float* srow = p.scores + g * p.stride_h + static_cast<int64_t>(i) * p.stride_t;
-  const bool cached = cur <= kCache;
   uint32_t* keys = s_keys[warp];
+  const bool cached = cur <= kCache;
   bool nan = false;
-  auto key_at = [&](int n) -> uint32_t {
-    return cached ? keys[n] : order_key(srow[n * p.stride_n], nan);
-  };
-  if (cached) {
-    for (int n = lane; n < cur; n += 32) keys[n] = order_key(srow[n * p.stride_n], nan);
-    __syncwarp();
-  }
+  auto load_key = [&](int n) -> uint32_t { return order_key(srow[n * p.stride_n], nan); };
 
-  int need = kTopK - 1;  // keys still to take among those matching the prefix
-  uint32_t prefix = 0, pmask = 0;
-  for (int shift = 28; shift >= 0; shift -= 4) {
-    if (lane < 16) s_hist[warp][lane] = 0;
+  // tau = the largest value with at least 15 keys >= tau (the 15th-largest key)
+  uint32_t tau = 0;
+  if (cur <= 32 * 8) {
+    tau = tau_in_registers<8>(load_key, keys, cur, lane);
+  } else if (cur <= 32 * kRegKeys) {
+    tau = tau_in_registers<kRegKeys>(load_key, keys, cur, lane);
+  } else {
+    if (cached)
+      for (int n = lane; n < cur; n += 32) keys[n] = load_key(n);
     __syncwarp();
-    for (int n = lane; n < cur; n += 32) {
-      const uint32_t k = key_at(n);
-      if ((k & pmask) == prefix) atomicAdd(&s_hist[warp][(k >> shift) & 15], 1);
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = tau | (1u << bit);
+      int cnt = 0;
+      for (int n = lane; n < cur; n += 32) cnt += ((cached ? keys[n] : load_key(n)) >= cand) ? 1 : 0;
+      if (__reduce_add_sync(0xffffffffu, cnt) >= kSel) tau = cand;
     }
-    __syncwarp();
-    // suffix[d] = number of matching keys whose digit is >= d
-    int suf = (lane < 16) ? s_hist[warp][lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) {
-      const int v = __shfl_down_sync(0xffffffffu, suf, off);
-      if (lane + off < 16) suf += v;
-    }
-    const unsigned ok = __ballot_sync(0xffffffffu, lane < 16 && suf >= need);
-    const int D = ok ? 31 - __clz(ok) : 0;          // largest digit reaching `need`
-    const int above = __shfl_sync(0xffffffffu, suf, (D + 1) & 31);
-    need -= (D < 15) ? above : 0;
-    prefix |= static_cast<uint32_t>(D) << shift;
-    pmask |= 15u << shift;
-    __syncwarp();
   }
-  const uint32_t tau = prefix;
+  __syncwarp();
+  auto key_at = [&](int n) -> uint32_t { return cached ? keys[n] : load_key(n); };
+  int gt_count = 0;
+  for (int n = lane; n < cur; n += 32) gt_count += (key_at(n) > tau) ? 1 : 0;
+  const int need = kSel - __reduce_add_sync(0xffffffffu, gt_count);  // ties to take, >= 1
 
   // keys > tau all kept; keys == tau kept in ascending index order until `need`
   int written = 0, ties = 0;
