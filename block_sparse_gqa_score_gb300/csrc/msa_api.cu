@@ -160,7 +160,7 @@ int msa_score(const void* q, const void* kv, const int32_t* block_table, const i
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.S = S;
-  p.chunk = (Q <= 4) ? 16 : 32;
+  p.ctas = dev->sm_count;
   p.num_blocks = num_blocks;
   p.scale = sm_scale * k_scale;
   return from_cuda(msa::launch_score(map, p, reinterpret_cast<cudaStream_t>(stream)));

@@ -452,8 +452,12 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   static_assert(smem <= 227 * 1024, "attend shared memory");
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
+    cudaError_t r = cudaFuncSetAttribute(attend_kernel<kAttendStages>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r != cudaSuccess) return r;
     return cudaFuncSetAttribute(attend_kernel<kAttendStages>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
   });
   if (e != cudaSuccess) return e;
   const int T = p.B * p.Q;

@@ -77,13 +77,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended (it issues nothing) for up
+// to `hint_ns` while the phase is incomplete; it resumes when the phase
+// completes or the hint expires.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity,
+                                                    unsigned hint_ns) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
-// Returns false on timeout (the caller flags MSA_ERR_TIMEOUT and bails out).
+// Waiting warps sleep inside try_wait instead of spinning, so they leave the
+// issue slots to the warps doing work.  Returns false on timeout (the caller
+// flags MSA_ERR_TIMEOUT and bails out).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  constexpr unsigned kHintNs = 1000000u;  // re-check the time limit every 1 ms at most
+  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
 }

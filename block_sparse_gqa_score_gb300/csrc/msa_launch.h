@@ -17,7 +17,7 @@ struct ScoreParams {
   float* scores;               // [Hkv, T, S]
   unsigned* err;               // device error word
   int B, Q, Hq, Hkv, S;
-  int chunk;                   // logical blocks per CTA
+  int ctas;                    // SM count (the scorer runs one or two CTAs per SM)
   int64_t num_blocks;
   float scale;                 // sm_scale * k_scale
 };

@@ -5,21 +5,27 @@
 // the query heads of g's group and the block's keys the token may see; -inf
 // past the token's current block and for padding rows.  Output [Hkv, T, S].
 //
-// Design (sm_103a, tcgen05): one CTA per (chunk of logical blocks, KV head,
-// request) -- a grid sized to the batch, not a 128-row query tile per token.
-//  * warp 0 streams the K halves (16 KiB per page-head) of the chunk's pages
-//    with TMA into 128B-swizzled stages;
+// Design (sm_103a, tcgen05, persistent): one or two CTAs per SM (two whenever
+// tensor and shared memory hold two pipelines).  The visible pages of
+// the batch, in (request, KV head, block) order, are split into equal
+// contiguous ranges, one per CTA; every CTA derives the same split from
+// seq_lens with a block-wide prefix sum, so no scratch memory or atomics are
+// needed and the grid stays fixed for a given shape.  Inside a CTA:
+//  * warp 0 streams the K halves (16 KiB per page-head) of its range with TMA
+//    into a ring of 128B-swizzled stages, from the first microseconds on;
 //  * warp 1 issues, from one thread, kind::f8f6f4 MMAs with the fp8 K tile
 //    straight from the TMA stage as operand A (M = 128 keys, K-major) and the
-//    request's Q x 16 query rows as operand B (N = 16 Q), accumulating fp32
-//    in tensor memory;
-//  * warps 2-5 read the accumulator from tensor memory (one key per lane),
-//    take the max over each token's 16 heads, apply the causal limit, and
-//    reduce over the 128 keys.
-// The bf16 query is represented exactly as the sum of two fp8 e4m3 parts
-// (q' = hi + lo after a per-token power-of-two scale; bf16's 8 significant
-// bits are 4 + 4), and both parts accumulate into the same tensor-memory
-// columns, so the fp8 keys need no widening at all.
+//    request's Q x 16 query rows as operand B (N = 16 Q), accumulating fp32 in
+//    double-buffered tensor memory;
+//  * warp 2 prepares the query tile of each (request, KV head) unit of the
+//    range: the bf16 query, scaled per token by a power of two 2^-e, is
+//    represented exactly as the sum of two fp8 e4m3 parts (bf16's 8
+//    significant bits are 4 + 4) that accumulate into the same columns, so
+//    the fp8 keys need no widening; it also writes the -inf tails;
+//  * warps 3-6 read the accumulator (one key per lane), take each token's max
+//    over its 16 heads and visible keys, and publish their four quarter-page
+//    maxima through shared memory and a per-slot mbarrier;
+//  * warp 7 combines the quarters and writes the scores.
 #include "msa_device.cuh"
 #include "msa_launch.h"
 #include "msa_tcgen05.cuh"
@@ -28,59 +34,66 @@ namespace msa {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
-constexpr int kEpiWarp0 = 2;
-constexpr int kMaxChunk = 32;
+constexpr int kThreads = 256;       // 8 warps, see above
+constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
+constexpr int kMaxStages = 8;
+constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
+constexpr int kQmulRing = 16;       // units whose scale factors are kept (> nqb + nacc + kRedSlots)
+constexpr int kSmemLimit = 227 * 1024;
 constexpr int kSmemPerSM = 233472;  // shared memory of one SM available to CTAs
 
 struct ScoreTail {
-  uint64_t full[kStages];   // TMA -> MMA
-  uint64_t empty[kStages];  // MMA -> TMA
-  uint64_t dfull[2];        // MMA -> epilogue (accumulator buffer ready)
-  uint64_t dempty[2];       // epilogue -> MMA (accumulator buffer drained)
-  uint64_t epi_done;        // epilogue warps finished their pages
-  uint64_t finish;          // every role finished (TMEM may be freed)
+  uint64_t full[kMaxStages];   // TMA -> MMA
+  uint64_t empty[kMaxStages];  // MMA -> TMA
+  uint64_t dfull[kMaxAcc];     // MMA -> epilogue (accumulator buffer ready)
+  uint64_t dempty[kMaxAcc];    // epilogue -> MMA (accumulator buffer drained)
+  uint64_t red_full[kRedSlots];   // epilogue -> combiner (four quarter maxima written)
+  uint64_t red_empty[kRedSlots];  // combiner -> epilogue (slot read)
+  uint64_t qfull[2];           // query prep -> MMA (query tile ready)
+  uint64_t qempty[2];          // MMA -> query prep (query tile no longer read)
+  uint64_t qmul_ready[kQmulRing];  // query prep -> epilogue (unit scale factors)
+  uint64_t finish;             // every role finished (TMEM may be freed)
   uint32_t tmem_base;
-  int n_pages;
-  int pages[kMaxChunk];
-  int loc[kMaxChunk];
+  int start_b, start_rem, count;   // this CTA's page range
+  int any_invalid;                 // some page of the range has a bad block-table entry
+  int64_t warp_sums[8];
 };
 
-static_assert(alignof(ScoreTail) <= 16, "tail alignment");
-
 struct ScoreGeometry {
-  int Q, chunk, nh, Qu, ncols;
-  int qtile_bytes;  // one of the hi / lo query tiles: 16 Q rows x 128 B
-  // byte offsets from the 1024-aligned base; every region starts 16-byte aligned
-  int off_qhi, off_qlo, off_qmul, off_red, off_tail;
-  int smem_needed, smem_request;
+  int Q, nh, Qu, nacc, ncols, nqb, stages, per_sm;
+  int qtile_bytes;  // hi + lo query tiles of one unit: 2 x 16Q rows x 128 B
+  int off_q, off_qmul, off_red, off_tail, smem;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-__host__ __device__ inline ScoreGeometry score_geometry(int Q, int chunk) {
+__host__ __device__ inline ScoreGeometry score_geometry(int Q) {
   ScoreGeometry G{};
   G.Q = Q;
-  G.chunk = chunk;
   G.nh = (16 * Q > 256) ? 2 : 1;        // MMA N is at most 256: split the tokens in two
   G.Qu = (Q + G.nh - 1) / G.nh;         // tokens per accumulator unit
-  int cols = 2 * 16 * G.Qu;             // two accumulator buffers
+  G.nacc = (kMaxAcc * 16 * G.Qu <= 256) ? kMaxAcc : 2;   // accumulator buffers
+  int cols = G.nacc * 16 * G.Qu;
   int nc = 32;
   while (nc < cols) nc <<= 1;
   G.ncols = nc;
-  G.qtile_bytes = 16 * Q * 128;
-  G.off_qhi = kStages * kHalfTile;
-  G.off_qlo = G.off_qhi + G.qtile_bytes;
-  G.off_qmul = G.off_qlo + G.qtile_bytes;
-  G.off_red = G.off_qmul + align16(Q * 4);
-  G.off_tail = G.off_red + align16(chunk * 4 * Q * 4);
-  G.smem_needed = G.off_tail + align16(static_cast<int>(sizeof(ScoreTail))) + 1024;
-  // ask for enough shared memory that no more CTAs share an SM than its
-  // tensor memory (512 columns) can hold at once
-  const int kmax = 512 / nc;
-  const int floor_bytes = kSmemPerSM / (kmax + 1) - 1024 + 16;
-  G.smem_request = G.smem_needed > floor_bytes ? G.smem_needed : floor_bytes;
+  G.qtile_bytes = 2 * 16 * Q * 128;
+  G.nqb = (2 * G.qtile_bytes <= 64 * 1024) ? 2 : 1;   // double-buffer small query tiles
+  const int fixed = G.nqb * G.qtile_bytes + align16(kQmulRing * Q * 4) +
+                    align16(kRedSlots * 4 * Q * 4) + align16(static_cast<int>(sizeof(ScoreTail))) +
+                    1024;
+  // two CTAs per SM (two independent pipelines) when tensor memory and shared
+  // memory hold two; each then gets half an SM's shared memory
+  const int two_budget = kSmemPerSM / 2 - 1024;
+  G.per_sm = (nc <= 256 && (two_budget - fixed) / kHalfTile >= 3) ? 2 : 1;
+  const int budget = G.per_sm == 2 ? two_budget : kSmemLimit;
+  int st = (budget - fixed) / kHalfTile;
+  G.stages = st > kMaxStages ? kMaxStages : st;
+  G.off_q = G.stages * kHalfTile;
+  G.off_qmul = G.off_q + G.nqb * G.qtile_bytes;
+  G.off_red = G.off_qmul + align16(kQmulRing * Q * 4);
+  G.off_tail = G.off_red + align16(kRedSlots * 4 * Q * 4);
+  G.smem = G.off_tail + align16(static_cast<int>(sizeof(ScoreTail))) + 1024;
   return G;
 }
 
@@ -93,88 +106,72 @@ __device__ __forceinline__ float order_float(int i) {
   return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+// Visible blocks of request b: ceil(seq_len / 128), or 0 for an empty or
+// inconsistent request (seq_len < 0 or more blocks than the table holds).
+__device__ __forceinline__ int visible_blocks(const ScoreParams& p, int b) {
+  const int L = p.seq_lens[b];
+  if (L <= 0 || (L - 1) / kPage >= p.S) return 0;
+  return (L - 1) / kPage + 1;
+}
+
+// Sequential walk over this CTA's pages in (request, KV head, block) order.
+struct PageWalk {
+  int b, g, n, nhi, L;
+  __device__ void load(const ScoreParams& p) {
+    L = p.seq_lens[b];
+    nhi = visible_blocks(p, b);
+  }
+  __device__ void begin(const ScoreParams& p, int b0, int rem) {
+    b = b0;
+    load(p);
+    g = rem / nhi;
+    n = rem - g * nhi;
+  }
+  // Move k pages forward (k >= 0), crossing requests as needed.
+  __device__ void advance(const ScoreParams& p, int64_t k) {
+    while (k > 0 && b < p.B) {
+      const int64_t here = static_cast<int64_t>(g) * nhi + n;
+      const int64_t left = static_cast<int64_t>(p.Hkv) * nhi - here;  // incl. the current page
+      if (k < left) {
+        const int64_t rem = here + k;
+        g = static_cast<int>(rem / nhi);
+        n = static_cast<int>(rem - static_cast<int64_t>(g) * nhi);
+        return;
+      }
+      k -= left;
+      g = 0;
+      n = 0;
+      do {
+        ++b;
+        if (b >= p.B) return;
+        load(p);
+      } while (nhi == 0);
+    }
+  }
+  __device__ void next(const ScoreParams& p) {
+    if (++n < nhi) return;
+    n = 0;
+    if (++g < p.Hkv) return;
+    g = 0;
+    do {
+      ++b;
+      if (b >= p.B) return;
+      load(p);
+    } while (nhi == 0);
+  }
+};
+
+__device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk& w, int& page) {
+  page = p.block_table[static_cast<int64_t>(w.b) * p.S + w.n];
+  return page >= 0 && static_cast<int64_t>(page) < p.num_blocks;
+}
+
+// Query tile of unit (b, g) into hi / lo (16 Q rows x 128 B each, 128B
+// swizzled, K-major), per-token factors scale * 2^e into qmul[0..Q).
+__device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
+                                   float* qmul, int lane) {
   const int Q = p.Q;
-  const ScoreGeometry G = score_geometry(Q, p.chunk);
-  uint8_t* stages = smem;                                         // [kStages][128][128 B]
-  uint8_t* qhi = smem + G.off_qhi;                                // [16Q][128 B] swizzled
-  uint8_t* qlo = smem + G.off_qlo;
-  float* qmul = reinterpret_cast<float*>(smem + G.off_qmul);      // [Q]
-  float* red = reinterpret_cast<float*>(smem + G.off_red);        // [chunk][4][Q]
-  ScoreTail* tail = reinterpret_cast<ScoreTail*>(smem + G.off_tail);
-
-  const int chunk = p.chunk;
-  const int n0 = blockIdx.x * chunk;
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = p.B * Q;
-
-  int L = p.seq_lens[b];
-  const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
-  if (!seq_ok) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
-    L = 0;
-  }
-  const int n_hi = min(min(n0 + chunk, p.S), (L >= 1) ? (L - 1) / kPage + 1 : 0);
-  const int n_end = min(n0 + chunk, p.S);
-
-  if (n0 >= n_hi) {
-    // nothing visible in this chunk: every score is -inf
-    for (int idx = threadIdx.x; idx < (n_end - n0) * Q; idx += kThreads) {
-      const int jq = idx / (n_end - n0), nl = idx - jq * (n_end - n0);
-      p.scores[(static_cast<int64_t>(g) * T + static_cast<int64_t>(b) * Q + jq) * p.S + n0 + nl] =
-          -INFINITY;
-    }
-    return;
-  }
-
-  for (int idx = threadIdx.x; idx < chunk * 4 * Q; idx += kThreads) red[idx] = -INFINITY;
-
-  if (warp == 0) {
-    // page list of the chunk
-    const int n = n0 + lane;
-    bool valid = false;
-    int page = -1;
-    if (lane < chunk && n < n_hi) {
-      page = p.block_table[static_cast<int64_t>(b) * p.S + n];
-      if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks)
-        flag_error(p.err, MSA_ERR_PAGE_RANGE);
-      else
-        valid = true;
-    }
-    const unsigned vm = __ballot_sync(0xffffffffu, valid);
-    if (valid) {
-      const int k = __popc(vm & ((1u << lane) - 1u));
-      tail->pages[k] = page;
-      tail->loc[k] = lane;
-    }
-    if (lane == 0) {
-      tail->n_pages = __popc(vm);
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(&tail->full[s], 1);
-        mbar_init(&tail->empty[s], 1);
-      }
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(&tail->dfull[s], 1);
-        mbar_init(&tail->dempty[s], 4);
-      }
-      mbar_init(&tail->epi_done, 4);
-      mbar_init(&tail->finish, 6);
-      fence_barrier_init();
-    }
-  } else if (warp == 1) {
-    tc::tmem_alloc(&tail->tmem_base, G.ncols);
-    tc::tmem_relinquish();
-  }
-
-  // ---- query tiles: per token, q' = q * 2^-e split into fp8 hi + lo -------------
-  // Token j's 16 heads are rows 16j..16j+15 of both tiles; lane = (head, half of d).
-  for (int jq = warp; jq < Q; jq += kThreads / 32) {
+  for (int jq = 0; jq < Q; ++jq) {
     const int r = lane >> 1, half = lane & 1;
     const uint16_t* src =
         p.q + ((static_cast<int64_t>(b) * Q + jq) * p.Hq + g * kGroup + r) * kHeadDim + 64 * half;
@@ -207,16 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 v = raw[el >> 3];
         const uint32_t pair0 = ((el & 7) == 0) ? v.x : v.z;
         const uint32_t pair1 = ((el & 7) == 0) ? v.y : v.w;
-        float x[4] = {bf16_bits_to_f32(pair0 & 0xFFFF) * sd, bf16_bits_to_f32(pair0 >> 16) * sd,
-                      bf16_bits_to_f32(pair1 & 0xFFFF) * sd, bf16_bits_to_f32(pair1 >> 16) * sd};
-        const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
-        uint32_t w01 = e4m3x2_to_f16x2(h01), w23 = e4m3x2_to_f16x2(h23);
-        const __half2 f01 = *reinterpret_cast<const __half2*>(&w01);
-        const __half2 f23 = *reinterpret_cast<const __half2*>(&w23);
-        const uint32_t l01 = f32x2_to_e4m3x2(x[0] - __low2float(f01), x[1] - __high2float(f01));
-        const uint32_t l23 = f32x2_to_e4m3x2(x[2] - __low2float(f23), x[3] - __high2float(f23));
-        hw[wi] = h01 | (h23 << 16);
-        lw[wi] = l01 | (l23 << 16);
+        const float x[4] = {bf16_bits_to_f32(pair0 & 0xFFFF) * sd,
+                            bf16_bits_to_f32(pair0 >> 16) * sd,
+                            bf16_bits_to_f32(pair1 & 0xFFFF) * sd,
+                            bf16_bits_to_f32(pair1 >> 16) * sd};
+        split_e4m3x4(x, hw[wi], lw[wi]);
       }
       const int off = sw128(R, 4 * half + c4);
       *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -224,50 +216,191 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) qmul[jq] = p.scale * exp2i(e);
   }
-  tc::fence_proxy_async_smem();   // query tiles are read by the tensor core
+}
+
+// At most 128 registers: registers are allocated per SM sub-partition (16K
+// each), so two 7-warp CTAs per SM need <= 128 per thread.
+__global__ void __maxnreg__(128)
+    score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int Q = p.Q;
+  const ScoreGeometry G = score_geometry(Q);
+  uint8_t* stages = smem;                                              // [stages][128][128 B]
+  uint8_t* qtiles = smem + G.off_q;                                    // [nqb][hi, lo][16Q][128 B]
+  float* qmul_ring = reinterpret_cast<float*>(smem + G.off_qmul);      // [kQmulRing][Q]
+  float* red = reinterpret_cast<float*>(smem + G.off_red);             // [kRedSlots][4][Q]
+  ScoreTail* tail = reinterpret_cast<ScoreTail*>(smem + G.off_tail);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int T = p.B * Q;
+  const int qtile_half = G.qtile_bytes / 2;
+
+  // ---- this CTA's page range: block-wide prefix sum over the requests -----------
+  {
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+    int64_t local = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int L = p.seq_lens[b];
+      if (blockIdx.x == 0 && (L < 0 || (L > 0 && (L - 1) / kPage >= p.S)))
+        flag_error(p.err, MSA_ERR_SEQ_RANGE);
+      local += static_cast<int64_t>(p.Hkv) * visible_blocks(p, b);
+    }
+    int64_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) tail->warp_sums[warp] = incl;
+    __syncthreads();
+    int64_t before = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) before += tail->warp_sums[w];
+      total += tail->warp_sums[w];
+    }
+    const int64_t excl = before + incl - local;
+    const int64_t w0 = total * blockIdx.x / gridDim.x, w1 = total * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) tail->count = static_cast<int>(w1 - w0);
+    if (w0 < w1 && excl <= w0 && w0 < excl + local) {
+      int64_t acc = excl;
+      for (int b = b_lo; b < b_hi; ++b) {
+        const int64_t pb = static_cast<int64_t>(p.Hkv) * visible_blocks(p, b);
+        if (w0 < acc + pb) {
+          tail->start_b = b;
+          tail->start_rem = static_cast<int>(w0 - acc);
+          break;
+        }
+        acc += pb;
+      }
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < G.stages; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], 1);
+    }
+    for (int s = 0; s < kMaxAcc; ++s) {
+      mbar_init(&tail->dfull[s], 1);
+      mbar_init(&tail->dempty[s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tail->qfull[s], 1);
+      mbar_init(&tail->qempty[s], 1);
+    }
+    for (int s = 0; s < kRedSlots; ++s) {
+      mbar_init(&tail->red_full[s], 4);
+      mbar_init(&tail->red_empty[s], 1);
+    }
+    for (int s = 0; s < kQmulRing; ++s) mbar_init(&tail->qmul_ready[s], 1);
+    mbar_init(&tail->finish, 8);
+    tail->any_invalid = 0;
+    fence_barrier_init();
+  } else if (warp == 1) {
+    tc::tmem_alloc(&tail->tmem_base, G.ncols);
+    tc::tmem_relinquish();
+  }
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
-  const int n_pages = tail->n_pages;
+  const int count = tail->count;
   const uint32_t tmem = tail->tmem_base;
 
+  // Warps 1 and 3-7 check every block-table entry of the range once, in
+  // parallel, while warp 0 starts streaming and warp 2 prepares the first
+  // query tile; when all are valid (the normal case) the MMA and epilogue
+  // roles need no per-page table reads on their critical path.
+  bool all_valid = true;
+  if (warp != 0 && warp != 2) {
+    const int nthr = kThreads - 64, t_id = tid - (warp == 1 ? 32 : 64);
+    const int t0 = static_cast<int>(static_cast<int64_t>(count) * t_id / nthr);
+    const int t1 = static_cast<int>(static_cast<int64_t>(count) * (t_id + 1) / nthr);
+    if (t0 < t1) {
+      PageWalk w;
+      w.begin(p, tail->start_b, tail->start_rem);
+      w.advance(p, t0);
+      bool bad = false;
+      for (int t = t0; t < t1; ++t, w.next(p)) {
+        int page;
+        bad |= !page_valid(p, w, page);
+      }
+      if (bad) atomicOr(&tail->any_invalid, 1);
+    }
+    named_barrier(2, kThreads - 64);   // no wait precedes it: warps 1, 3-7 all arrive
+    all_valid = *reinterpret_cast<volatile int*>(&tail->any_invalid) == 0;
+  }
+
   if (warp == 0) {
-    // ---- TMA producer ----------------------------------------------------------
+    // ---- TMA producer ------------------------------------------------------------
     if (lane == 0) {
       prefetch_tensormap(&kv_map);
-      int issued = 0;
-      for (int t = 0; t < n_pages; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&tail->empty[s], ((t / kStages) - 1) & 1)) {
+      PageWalk w;
+      if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+      int vp = 0;
+      for (int t = 0; t < count; ++t, w.next(p)) {
+        int page;
+        if (!page_valid(p, w, page)) {
+          if (p.err) flag_error(p.err, MSA_ERR_PAGE_RANGE);
+          continue;
+        }
+        const int s = vp % G.stages;
+        if (vp >= G.stages && !mbar_wait(&tail->empty[s], ((vp / G.stages) - 1) & 1)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
         mbar_arrive_expect_tx(&tail->full[s], kHalfTile);
-        tma_load_2d(stages + s * kHalfTile, &kv_map, 0, (tail->pages[t] * p.Hkv + g) * kPage,
+        tma_load_2d(stages + s * kHalfTile, &kv_map, 0, (page * p.Hkv + w.g) * kPage,
                     &tail->full[s]);
-        ++issued;
+        ++vp;
       }
       // the last loads in flight land before shared memory can be released
-      for (int t = issued - kStages; t < issued; ++t)
-        if (t >= 0) (void)mbar_wait(&tail->full[t % kStages], (t / kStages) & 1);
+      for (int t = vp - G.stages; t < vp; ++t)
+        if (t >= 0) (void)mbar_wait(&tail->full[t % G.stages], (t / G.stages) & 1);
       mbar_arrive(&tail->finish);
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----------------------------------------------------------------
     if (lane == 0) {
-      const uint32_t stage_addr = smem_u32(stages);
-      const uint32_t qhi_addr = smem_u32(qhi), qlo_addr = smem_u32(qlo);
-      bool ok = true;
-      for (int t = 0; t < n_pages && ok; ++t) {
-        const int s = t % kStages;
-        if (!mbar_wait(&tail->full[s], (t / kStages) & 1)) {
+      // descriptors are built once and advanced by constants: the start
+      // address field counts 16-byte units (stage = 1024, k-step = 2)
+      const uint64_t adesc0 = tc::sw128_kmajor_desc(smem_u32(stages));
+      const uint64_t bdesc0 = tc::sw128_kmajor_desc(smem_u32(qtiles));
+      const uint64_t lo_step = static_cast<uint64_t>(qtile_half >> 4);
+      uint32_t idesc[2];
+      for (int h = 0; h < 2; ++h) idesc[h] = tc::idesc_e4m3_f32(128, 16 * max(1, min(G.Qu, Q - h * G.Qu)));
+      PageWalk w;
+      if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+      int k = -1, pb = -1, pg = -1, vp = 0;
+      bool q_ready = false, ok = true;
+      for (int t = 0; t < count && ok; ++t, w.next(p)) {
+        if (w.b != pb || w.g != pg) {
+          if (k >= 0) tc::commit(&tail->qempty[k % G.nqb]);  // old tile free once its MMAs end
+          ++k;
+          pb = w.b;
+          pg = w.g;
+          q_ready = false;
+        }
+        int page;
+        if (!all_valid && !page_valid(p, w, page)) continue;
+        if (!q_ready) {
+          if (!mbar_wait(&tail->qfull[k % G.nqb], (k / G.nqb) & 1)) {
+            flag_error(p.err, MSA_ERR_TIMEOUT);
+            break;
+          }
+          tc::fence_after_thread_sync();
+          q_ready = true;
+        }
+        const int s = vp % G.stages;
+        if (!mbar_wait(&tail->full[s], (vp / G.stages) & 1)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
         tc::fence_after_thread_sync();
-        const uint32_t a_base = stage_addr + s * kHalfTile;
+        const uint64_t a = adesc0 + static_cast<uint64_t>(s) * (kHalfTile >> 4);
+        const uint64_t bq = bdesc0 + static_cast<uint64_t>((k % G.nqb) * (G.qtile_bytes >> 4));
         for (int h = 0; h < G.nh; ++h) {
-          const int u = t * G.nh + h, buf = u & 1, use = u >> 1;
+          const int u = vp * G.nh + h, buf = u % G.nacc, use = u / G.nacc;
           if (use >= 1) {
             if (!mbar_wait(&tail->dempty[buf], (use - 1) & 1)) {
               flag_error(p.err, MSA_ERR_TIMEOUT);
@@ -276,21 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_after_thread_sync();
           }
-          const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
-          const uint32_t idesc = tc::idesc_e4m3_f32(128, 16 * ntok);
           const uint32_t d = tmem + buf * 16 * G.Qu;
-          const uint32_t b_off = tok0 * kGroup * 128;
+          const uint64_t bh = bq + static_cast<uint64_t>((h * G.Qu * kGroup * 128) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bh + 2 * ks, idesc[h], ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_e4m3(d, tc::sw128_kmajor_desc(a_base + 32 * ks),
-                         tc::sw128_kmajor_desc(qhi_addr + b_off + 32 * ks), idesc, ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_e4m3(d, tc::sw128_kmajor_desc(a_base + 32 * ks),
-                         tc::sw128_kmajor_desc(qlo_addr + b_off + 32 * ks), idesc, 1);
+            tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
           tc::commit(&tail->dfull[buf]);
         }
         tc::commit(&tail->empty[s]);
+        ++vp;
       }
       mbar_arrive(&tail->finish);
     }
@@ -299,17 +428,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     (void)mbar_wait(&tail->finish, 0);
     tc::fence_after_thread_sync();
     tc::tmem_dealloc(tmem, G.ncols);
-  } else {
+  } else if (warp == 2) {
+    // ---- query tiles, then the -inf tails ----------------------------------------------
+    PageWalk w;
+    if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+    int t = 0, k = 0;
+    bool ok = true;
+    while (t < count && ok) {
+      const int qb = k % G.nqb;
+      if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], ((k / G.nqb) - 1) & 1)) {
+        if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      uint8_t* qhi = qtiles + qb * G.qtile_bytes;
+      float* qmul = qmul_ring + (k % kQmulRing) * Q;
+      prepare_query_tile(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane);
+      tc::fence_proxy_async_smem();   // the tile is read by the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tail->qfull[qb]);
+        mbar_arrive(&tail->qmul_ready[k % kQmulRing]);
+      }
+      // skip to the first page of the next unit
+      const int in_unit = w.nhi - w.n;
+      for (int s = 0; s < in_unit && t < count; ++s, ++t) w.next(p);
+      ++k;
+    }
+    // -inf for blocks past each request's last visible block (units dealt
+    // round-robin over the CTAs; disjoint from every page written above)
+    for (int64_t u = blockIdx.x; u < static_cast<int64_t>(p.B) * p.Hkv; u += gridDim.x) {
+      const int b = static_cast<int>(u / p.Hkv), g = static_cast<int>(u - static_cast<int64_t>(b) * p.Hkv);
+      const int nhi = visible_blocks(p, b);
+      const int width = p.S - nhi;
+      for (int idx = lane; idx < width * Q; idx += 32) {
+        const int jq = idx / width, n = nhi + (idx - jq * width);
+        p.scores[(static_cast<int64_t>(g) * T + static_cast<int64_t>(b) * Q + jq) * p.S + n] =
+            -INFINITY;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->finish);
+  } else if (warp != 7) {
     // ---- epilogue: accumulator -> per-token block maxima ----------------------------
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
     const int key = 32 * quarter + lane;         // key (row of the page) of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+    PageWalk w;
+    if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+    int vp = 0;
     bool ok = true;
-    for (int t = 0; t < n_pages && ok; ++t) {
-      const int nl = tail->loc[t];
-      const int lim_base = L - Q - (n0 + nl) * kPage;   // token j sees keys <= lim_base + j
-      for (int h = 0; h < G.nh; ++h) {
-        const int u = t * G.nh + h, buf = u & 1, use = u >> 1;
+    for (int t = 0; t < count && ok; ++t, w.next(p)) {
+      int page;
+      if (!all_valid && !page_valid(p, w, page)) continue;
+      const int lim_base = w.L - Q - w.n * kPage;   // token j sees keys <= lim_base + j
+      float myv = -INFINITY;                        // lane jq: this quarter's max of token jq
+      for (int h = 0; h < G.nh && ok; ++h) {
+        const int u = vp * G.nh + h, buf = u % G.nacc, use = u / G.nacc;
         if (!mbar_wait(&tail->dfull[buf], use & 1)) {
           if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
           ok = false;
@@ -317,42 +492,94 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_thread_sync();
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
-        for (int jj = 0; jj < ntok; ++jj) {
-          const int jq = tok0 + jj;
-          const int lim = lim_base + jq;
-          if (lim < 0) continue;                 // warp-uniform: token sees nothing here
-          uint32_t v[16];
-          tc::ld_32x32b_x16(lane_addr + buf * 16 * G.Qu + jj * 16, v);
-          tc::wait_ld();
-          float m = __uint_as_float(v[0]);
+        // groups of four tokens: four TMEM loads in flight under one wait, then
+        // four independent tree maxima and four back-to-back warp reductions
+        for (int j0 = 0; j0 < ntok; j0 += 4) {
+          const int nj = min(4, ntok - j0);
+          if (lim_base + tok0 + j0 + nj - 1 < 0) continue;   // warp-uniform: nothing visible
+          uint32_t v[4][16];
 #pragma unroll
-          for (int e = 1; e < 16; ++e) m = fmaxf(m, __uint_as_float(v[e]));
-          if (key > lim) m = -INFINITY;
-          const float wmax = order_float(__reduce_max_sync(0xffffffffu, order_int(m)));
-          if (lane == 0) red[(nl * 4 + quarter) * Q + jq] = wmax;
+          for (int jj = 0; jj < 4; ++jj)
+            if (jj < nj) tc::ld_32x32b_x16(lane_addr + buf * 16 * G.Qu + (j0 + jj) * 16, v[jj]);
+          tc::wait_ld();
+          int ord[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              m8[e] = fmaxf(__uint_as_float(v[jj][e]), __uint_as_float(v[jj][e + 8]));
+            const float m = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const int lim = lim_base + tok0 + j0 + jj;
+            ord[jj] = order_int((jj < nj && key <= lim) ? m : -INFINITY);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) ord[jj] = __reduce_max_sync(0xffffffffu, ord[jj]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            if (jj < nj && lane == tok0 + j0 + jj) myv = order_float(ord[jj]);
         }
         tc::fence_before_thread_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tail->dempty[buf]);
       }
+      if (!ok) break;
+      // publish this quarter's maxima to the combiner
+      const int slot = vp % kRedSlots;
+      if (vp >= kRedSlots && !mbar_wait(&tail->red_empty[slot], ((vp / kRedSlots) - 1) & 1)) {
+        if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
+        break;
+      }
+      if (lane < Q) red[(slot * 4 + quarter) * Q + lane] = myv;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->red_full[slot]);
+      ++vp;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&tail->epi_done);
-    const bool all_done = mbar_wait(&tail->epi_done, 0);
-    if (all_done && ok) {
-      // write the chunk's scores for every token (blocks not computed: -inf)
-      const int et = threadIdx.x - kEpiWarp0 * 32;
-      for (int idx = et; idx < (n_end - n0) * Q; idx += 128) {
-        const int jq = idx / (n_end - n0), nl = idx - jq * (n_end - n0);
+    if (lane == 0) mbar_arrive(&tail->finish);
+  } else {
+    // ---- combiner: four quarters -> scores ---------------------------------------------
+    PageWalk w;
+    if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+    int k = -1, pb = -1, pg = -1, vp = 0;
+    float qm = 0.f;                              // scale of token `lane` of the current unit
+    bool have_qm = false;
+    for (int t = 0; t < count; ++t, w.next(p)) {
+      if (w.b != pb || w.g != pg) {
+        ++k;
+        pb = w.b;
+        pg = w.g;
+        have_qm = false;
+      }
+      const int64_t row0 = (static_cast<int64_t>(w.g) * T + static_cast<int64_t>(w.b) * Q) * p.S + w.n;
+      int page;
+      if (!all_valid && !page_valid(p, w, page)) {
+        if (lane < Q) p.scores[row0 + static_cast<int64_t>(lane) * p.S] = -INFINITY;
+        continue;
+      }
+      if (!have_qm) {
+        if (!mbar_wait(&tail->qmul_ready[k % kQmulRing], (k / kQmulRing) & 1)) {
+          if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
+          break;
+        }
+        qm = lane < Q ? qmul_ring[(k % kQmulRing) * Q + lane] : 0.f;
+        have_qm = true;
+      }
+      const int slot = vp % kRedSlots;
+      if (!mbar_wait(&tail->red_full[slot], (vp / kRedSlots) & 1)) {
+        if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
+        break;
+      }
+      if (lane < Q) {
         float v = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) v = fmaxf(v, red[(nl * 4 + w) * Q + jq]);
-        if (v != -INFINITY) v *= qmul[jq];
-        p.scores[(static_cast<int64_t>(g) * T + static_cast<int64_t>(b) * Q + jq) * p.S + n0 + nl] =
-            v;
+        for (int q4 = 0; q4 < 4; ++q4) v = fmaxf(v, red[(slot * 4 + q4) * Q + lane]);
+        p.scores[row0 + static_cast<int64_t>(lane) * p.S] = (v == -INFINITY) ? v : v * qm;
       }
-    } else if (!all_done && lane == 0) {
-      flag_error(p.err, MSA_ERR_TIMEOUT);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->red_empty[slot]);
+      ++vp;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&tail->finish);
@@ -362,17 +589,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream) {
-  if (p.chunk < 1 || p.chunk > kMaxChunk) return cudaErrorInvalidValue;
-  const ScoreGeometry G = score_geometry(p.Q, p.chunk);
-  if (G.smem_request > 227 * 1024) return cudaErrorInvalidValue;
+  if (p.ctas < 1) return cudaErrorInvalidValue;
+  const ScoreGeometry G = score_geometry(p.Q);
+  if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                227 * 1024);
+    cudaError_t r = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemLimit);
+    if (r != cudaSuccess) return r;
+    // all of the unified L1 / shared storage as shared memory, so that two
+    // CTAs of ~100 KB can be resident on one SM
+    return cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
   });
   if (e != cudaSuccess) return e;
-  dim3 grid((p.S + p.chunk - 1) / p.chunk, p.Hkv, p.B);
-  score_kernel<<<grid, kThreads, G.smem_request, stream>>>(kv_map, p);
+  score_kernel<<<p.ctas * G.per_sm, kThreads, G.smem, stream>>>(kv_map, p);
   return cudaGetLastError();
 }
 
