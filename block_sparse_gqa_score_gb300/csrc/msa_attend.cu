@@ -7,64 +7,99 @@
 // commit: "zeroed (not NaN) output for graph padding rows", fp32 split-K
 // partials).
 //
-// Design (sm_103a):
-//  * One CTA per (query token, KV head, split).  The token's 16 query heads of
-//    the group form exactly one m16 tile of the MMA, so no rows are wasted and
-//    pages are fetched per token; pages shared by the Q tokens of a request
-//    are deduplicated by L2, since the tokens' CTAs run side by side.
-//  * A producer warp streams each selected page-head (K half and V half, 16 KiB
-//    each) with two TMA tile loads into a ring of 128B-swizzled shared-memory
-//    stages; four compute warps each take 32 of the page's 128 keys.
-//  * fp8 K/V bytes are widened to fp16 in registers (cvt.rn.f16x2.e4m3x2) while
-//    building the MMA B fragments, so shared memory holds only the raw page.
-//  * Each warp keeps its own online-softmax state (m, l, O) over its keys; the
-//    four states are merged through shared memory at the end.
+// Design (sm_103a, tcgen05): one CTA per (query token, KV head, split).  The
+// token's 16 query heads are the N = 16 columns of two tensor-core products
+// taken transposed, so that the page's 128 keys, then its 128 value dims, fill
+// the M = 128 rows of the MMA:
+//   S^T = K Q^T    A = the fp8 K tile straight from the TMA stage (K-major);
+//                  B = the query, scaled by a power of two and split exactly
+//                  into fp8 e4m3 hi and lo parts, side by side as N = 32
+//   O^T = V^T P^T  A = the fp8 V tile of the same stage, read MN-major, i.e.
+//                  as stored; B = the probabilities split into e4m3 hi and lo
+//                  parts, again side by side as N = 32
+// both kind::f8f6f4 with fp32 accumulators in tensor memory (the softmax
+// threads add the hi and lo columns), so no fp8 value is widened in
+// registers and a page takes 4 + 4 MMAs.  Warp roles:
+//   0    TMA producer: each selected page-head (K and V halves, 32 KiB) into a
+//        3-stage ring of 128B-swizzled tiles;
+//   1    issues S^T (and owns tensor memory); 2 issues O^T;
+//   3-6  softmax.  A thread owns one key of the page (one TMEM lane of S^T):
+//        the page's per-head maxima come from warp reductions and a
+//        four-warp exchange; the reference m of a head moves only when a page
+//        exceeds it by more than half a binade, so P = 2^(x - m + 8) stays
+//        below 2^8.5 (the e4m3 range keeps 17 binades below it) and the
+//        rescale factors are 1 on most pages; each thread keeps its share of
+//        the running sums.  When a page's O^T is ready the same
+//        thread owns one value dim d (one TMEM lane of O^T) and accumulates
+//        O = O * alpha + O_page in registers, so O is never rescaled in place.
 #include "msa_device.cuh"
 #include "msa_launch.h"
+#include "msa_tcgen05.cuh"
 
 namespace msa {
 
 namespace {
 
-constexpr int kComputeWarps = 4;
-constexpr int kThreads = (kComputeWarps + 1) * 32;
-constexpr int kStageBytes = 2 * kHalfTile;  // K tile then V tile
+constexpr int kStages = 3;
+constexpr int kWarps = 7;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSoftmaxWarp0 = 3;              // warps 3..6; warp w reads TMEM lanes 32*(w%4)..
+constexpr int kStageBytes = 2 * kHalfTile;    // K tile then V tile
+constexpr int kQPart = kGroup * 128;          // one fp8 part of the query tile: 16 rows x 128 B
+constexpr int kPPart = kPage * kGroup;        // one fp8 part of P^T: 128 keys x 16 heads
+// P^T buffer: per block of 8 keys, the hi part's 8 x 16 B core matrix, then
+// the lo part's (256 B per block, 2 * kPPart per buffer)
+constexpr int kPBlock = 256;
+constexpr int kTmemCols = 128;                // S^T x 2 buffers, O^T x 2 buffers, 32 columns each
+constexpr uint32_t kColS = 0, kColO = 64;
+constexpr float kPShift = 8.f;                // P = 2^(x - m + kPShift)
+constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it by more than this
 
-struct AttendSmemTail {
-  uint64_t full[8];
-  uint64_t empty[8];
-  uint64_t drained;  // the compute warps are done with the stage ring
-  uint64_t merged;   // the compute warps have written their softmax states
-  int abort;         // set by a warp whose wait timed out
+struct AttendTail {
+  uint64_t full[kStages];   // TMA -> S^T issuer
+  uint64_t empty[kStages];  // O^T issuer (stage's last reader) -> TMA
+  uint64_t s_full[2];       // S^T ready -> softmax
+  uint64_t s_empty[2];      // softmax has read S^T -> S^T issuer
+  uint64_t p_full[2];       // P^T written -> O^T issuer
+  uint64_t o_full[2];       // O^T ready -> softmax
+  uint64_t o_empty[2];      // softmax has read O^T -> O^T issuer
+  uint64_t mx_full[2];      // the four softmax warps' page maxima written
+  uint64_t l_full;          // the four softmax warps' running sums written
+  uint64_t finish;          // every role done and every MMA complete
+  uint32_t tmem_base;
+  int n_pages, pos;
+  float zs;                 // logit scale (log2 units) times 2^e of the query split
   int pages[kTopK];
   int blocks[kTopK];
-  int n_pages;
-  int pos;
 };
 
-// fp16 query fragments shared by the compute warps: [k-step][lane] uint4
-constexpr int kQfragBytes = 8 * 32 * 16;
-constexpr int kTailBytes = static_cast<int>((sizeof(AttendSmemTail) + 15) / 16 * 16);
+// shared-memory layout (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = kStages * kStageBytes;        // query hi, lo
+constexpr int kOffP = kOffQ + 2 * kQPart;           // P^T [2 buffers], see kPBlock
+constexpr int kOffMx = kOffP + 4 * kPPart;          // page maxima [2][4 warps][16]
+constexpr int kOffL = kOffMx + 2 * 4 * kGroup * 4;  // running sums [4 warps][16]
+constexpr int kOffTail = kOffL + 4 * kGroup * 4;
+constexpr int kSmemBytes = kOffTail + static_cast<int>((sizeof(AttendTail) + 15) / 16 * 16) + 1024;
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(kOffTail % 16 == 0, "mbarriers need 8-byte alignment");
 
-template <int NST>
-constexpr int attend_smem_bytes() {
-  return NST * kStageBytes + kTailBytes + kQfragBytes + 1024;
+template <int N>
+__device__ __forceinline__ void fill(float (&a)[N], float v) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) a[k] = v;
 }
 
-// Returns the PRMT selector that gathers byte r of x and byte r of y into the
-// low two bytes of the result.
-__device__ __forceinline__ uint32_t pair_bytes(uint32_t x, uint32_t y, int r) {
-  return __byte_perm(x, y, static_cast<uint32_t>(r | ((r + 4) << 4)));
-}
-
-template <int NST>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap kv_map, const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  AttendSmemTail* tail = reinterpret_cast<AttendSmemTail*>(smem + NST * kStageBytes);
-  uint4* qfrag = reinterpret_cast<uint4*>(smem + NST * kStageBytes + kTailBytes);  // [8][32]
+  AttendTail* tail = reinterpret_cast<AttendTail*>(smem + kOffTail);
+  uint8_t* qhi = smem + kOffQ;
+  uint8_t* qlo = qhi + kQPart;
+  uint8_t* pbuf = smem + kOffP;
+  float* mx = reinterpret_cast<float*>(smem + kOffMx);
+  float* lsum = reinterpret_cast<float*>(smem + kOffL);
 
   const int i = blockIdx.x;      // query token
   const int g = blockIdx.y;      // KV head
@@ -72,8 +107,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = i / p.Q, j = i - b * p.Q;
 
-  // ---- prologue: the producer warp resolves this CTA's page list ----------
-  if (warp == kComputeWarps) {
+  // ---- prologue ------------------------------------------------------------------
+  if (warp == 0) {
+    // this CTA's page list, barriers, and the first loads
     const int L = p.seq_lens[b];
     const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
@@ -111,31 +147,58 @@ __global__ void __launch_bounds__(kThreads, 2)
       tail->pages[k] = page;
       tail->blocks[k] = n;
     }
+    __syncwarp();
     if (lane == 0) {
-      tail->n_pages = __popc(mm);
+      const int np = __popc(mm);
+      tail->n_pages = np;
       tail->pos = pos;
-      for (int s = 0; s < NST; ++s) {
+      for (int s = 0; s < kStages; ++s) {
         mbar_init(&tail->full[s], 1);
-        mbar_init(&tail->empty[s], kComputeWarps);
+        mbar_init(&tail->empty[s], 1);
       }
-      mbar_init(&tail->drained, kComputeWarps);
-      mbar_init(&tail->merged, kComputeWarps);
-      tail->abort = 0;
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&tail->s_full[s], 1);
+        mbar_init(&tail->s_empty[s], 4);
+        mbar_init(&tail->p_full[s], 4);
+        mbar_init(&tail->o_full[s], 1);
+        mbar_init(&tail->o_empty[s], 4);
+        mbar_init(&tail->mx_full[s], 4);
+      }
+      mbar_init(&tail->l_full, 4);
+      mbar_init(&tail->finish, kWarps);
       fence_barrier_init();
+      prefetch_tensormap(&kv_map);
+      for (int t = 0; t < np && t < kStages; ++t) {
+        uint8_t* st = smem + t * kStageBytes;
+        const int row = (tail->pages[t] * p.Hkv + g) * kPage;
+        mbar_arrive_expect_tx(&tail->full[t], kStageBytes);
+        tma_load_2d(st, &kv_map, 0, row, &tail->full[t]);
+        tma_load_2d(st + kHalfTile, &kv_map, kHeadDim, row, &tail->full[t]);
+      }
     }
+  } else if (warp == 1) {
+    tc::tmem_alloc(&tail->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  } else if (warp == kSoftmaxWarp0) {
+    const int e = prepare_query_e4m3(p.q + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim,
+                                     0, qhi, qlo, lane);
+    tc::fence_proxy_async_smem();  // the tiles are read by the tensor core
+    if (lane == 0) tail->zs = p.logit_scale * exp2i(e);
   }
+  tc::fence_before_thread_sync();
   __syncthreads();
+  tc::fence_after_thread_sync();
   const int n_pages = tail->n_pages;
   const int pos = tail->pos;
+  const uint32_t tmem = tail->tmem_base;
 
-  if (warp == kComputeWarps) {
-    // ---- producer: stream the selected page-heads through the stage ring ----
+  if (warp == 0) {
+    // ---- TMA producer ------------------------------------------------------------------
     if (lane == 0) {
-      prefetch_tensormap(&kv_map);
-      int issued = 0;
-      for (int t = 0; t < n_pages; ++t) {
-        const int s = t % NST;
-        if (t >= NST && !mbar_wait(&tail->empty[s], ((t / NST) - 1) & 1)) {
+      int issued = n_pages < kStages ? n_pages : kStages;
+      for (int t = kStages; t < n_pages; ++t) {
+        const int s = t % kStages;
+        if (!mbar_wait(&tail->empty[s], ((t / kStages) - 1) & 1)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
@@ -144,269 +207,283 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(&tail->full[s], kStageBytes);
         tma_load_2d(st, &kv_map, 0, row, &tail->full[s]);
         tma_load_2d(st + kHalfTile, &kv_map, kHeadDim, row, &tail->full[s]);
-        ++issued;
+        issued = t + 1;
       }
-      (void)issued;
+      // the loads still in flight land before shared memory can be released
+      for (int t = issued - kStages; t < issued; ++t)
+        if (t >= 0) (void)mbar_wait(&tail->full[t % kStages], (t / kStages) & 1);
+      mbar_arrive(&tail->finish);
     }
-    return;
-  }
-
-  // ---- compute warps ---------------------------------------------------------
-  const int gr = lane >> 2, c = lane & 3;
-  const int key0 = warp * 32;
-  float zs0, zs1;  // logit scales (log2 units) of rows gr / gr+8, times their power-of-two factors
-  {
-    // every warp prepares the fp16 query fragments; warp w stores k-steps 2w, 2w+1
-    uint32_t qa[8][4];
-    load_query_fragments(p.q + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim, lane,
-                         p.logit_scale, qa, zs0, zs1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      if ((ks >> 1) == warp)
-        qfrag[ks * 32 + lane] = make_uint4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-  }
-  named_barrier(1, kComputeWarps * 32);  // no wait precedes it: every compute warp arrives
-
-  // m0/m1: the reference maximum used for rows gr / gr+8 (lazily raised: it
-  // only moves when a page's maximum exceeds it by more than kLazy, so the
-  // probabilities stay <= 2^kLazy, well inside fp16).
-  constexpr float kLazy = 8.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[16][4];
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
-
-  bool timed_out = false;
-  int consumed = 0;
-  for (int t = 0; t < n_pages; ++t) {
-    const int s = t % NST;
-    if (!mbar_wait(&tail->full[s], (t / NST) & 1)) {
-      if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
-      timed_out = true;
-      break;
-    }
-    consumed = t + 1;
-    const uint8_t* kt = smem + s * kStageBytes;
-    const uint8_t* vt = kt + kHalfTile;
-    const int lim = pos - tail->blocks[t] * kPage;  // keys <= lim are visible
-    const bool whole = lim >= kPage - 1;            // same for the whole CTA
-
-    // S = Q K^T (fp16 MMA; fp8 keys widened in registers)
-    float acc[4][4];
-#pragma unroll
-    for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[tt][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint4 qv = qfrag[ks * 32 + lane];
-      const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
-        const int row = key0 + 8 * tt + gr;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + sw128(row, ks) + 4 * c);
-        mma_f16(acc[tt], qa, e4m3x2_to_f16x2(w & 0xFFFF), e4m3x2_to_f16x2(w >> 16));
-      }
-    }
-    if (!whole) {
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
-        const int key = key0 + 8 * tt + 2 * c;
-        if (key > lim) acc[tt][0] = acc[tt][2] = -INFINITY;
-        if (key + 1 > lim) acc[tt][1] = acc[tt][3] = -INFINITY;
-      }
-    }
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
-      mx0 = fmaxf(mx0, fmaxf(acc[tt][0], acc[tt][1]));
-      mx1 = fmaxf(mx1, fmaxf(acc[tt][2], acc[tt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mz0 = mx0 * zs0, mz1 = mx1 * zs1;   // page maxima in log2 units
-    const bool r0 = mz0 > m0 + kLazy, r1 = mz1 > m1 + kLazy;
-    if (__any_sync(0xffffffffu, r0 || r1)) {
-      const float al0 = r0 ? ex2(m0 - mz0) : 1.f;  // ex2(-inf) = 0 on the first raise
-      const float al1 = r1 ? ex2(m1 - mz1) : 1.f;
-      if (r0) m0 = mz0;
-      if (r1) m1 = mz1;
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int dt = 0; dt < 16; ++dt) {
-        o[dt][0] *= al0;
-        o[dt][1] *= al0;
-        o[dt][2] *= al1;
-        o[dt][3] *= al1;
-      }
-    }
-    // p = 2^(acc*zs - m); a row with no visible key yet has m = -inf and only
-    // -inf logits, which give 0
-    const float nm0 = (m0 == -INFINITY) ? 0.f : -m0;
-    const float nm1 = (m1 == -INFINITY) ? 0.f : -m1;
-    uint32_t pa[2][4];
-#pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
-      const float p0 = ex2(fmaf(acc[tt][0], zs0, nm0)), p1 = ex2(fmaf(acc[tt][1], zs0, nm0));
-      const float p2 = ex2(fmaf(acc[tt][2], zs1, nm1)), p3 = ex2(fmaf(acc[tt][3], zs1, nm1));
-      l0 += p0 + p1;
-      l1 += p2 + p3;
-      // C fragments of key tiles (2k, 2k+1) form the A fragment of PV k-step k
-      pa[tt >> 1][(tt & 1) * 2 + 0] = pack_f16x2(p0, p1);
-      pa[tt >> 1][(tt & 1) * 2 + 1] = pack_f16x2(p2, p3);
-    }
-
-    // O += P V (fp16 MMA).  Logical d-column n of d-tile 4*q4 + r is physical
-    // d = 4*(n + 8*q4) + r, so each lane's 4-byte load of one V row covers
-    // four d-tiles; rows 2c, 2c+1, 2c+8, 2c+9 of the k-step give the B pairs.
-    // On the current block's page, rows past the causal limit are zeroed so
-    // that whatever bytes they hold cannot reach the output.
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int rb = key0 + 16 * kk + 2 * c;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int chunk = (gr >> 2) + 2 * q4;
-        const int word = 4 * (gr & 3);
-        uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb, chunk) + word);
-        uint32_t w1 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 1, chunk) + word);
-        uint32_t w2 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 8, chunk) + word);
-        uint32_t w3 = *reinterpret_cast<const uint32_t*>(vt + sw128(rb + 9, chunk) + word);
-        if (!whole) {
-          if (rb > lim) w0 = 0u;
-          if (rb + 1 > lim) w1 = 0u;
-          if (rb + 8 > lim) w2 = 0u;
-          if (rb + 9 > lim) w3 = 0u;
+  } else if (warp == 1) {
+    // ---- S^T = K Q^T ------------------------------------------------------------------------
+    if (lane == 0) {
+      // B: 32 rows, the hi part (rows 0-15) directly followed by the lo part
+      const uint64_t a0 = tc::sw128_kmajor_desc(smem_u32(smem));
+      const uint64_t bq = tc::sw128_kmajor_desc(smem_u32(qhi));
+      constexpr uint32_t idesc = tc::idesc_e4m3_f32(128, 2 * kGroup);
+      for (int t = 0; t < n_pages; ++t) {
+        const int s = t % kStages, buf = t & 1;
+        if (!mbar_wait(&tail->full[s], (t / kStages) & 1) ||
+            (t >= 2 && !mbar_wait(&tail->s_empty[buf], ((t >> 1) - 1) & 1))) {
+          flag_error(p.err, MSA_ERR_TIMEOUT);
+          break;
         }
+        tc::fence_after_thread_sync();
+        const uint64_t a = a0 + static_cast<uint64_t>(s) * (kStageBytes >> 4);
+        const uint32_t d = tmem + kColS + 2 * kGroup * buf;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t b0 = e4m3x2_to_f16x2(pair_bytes(w0, w1, r));
-          const uint32_t b1 = e4m3x2_to_f16x2(pair_bytes(w2, w3, r));
-          mma_f16(o[4 * q4 + r], pa[kk], b0, b1);
-        }
+        for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bq + 2 * ks, idesc, ks > 0);
+        tc::commit(&tail->s_full[buf]);
       }
+      tc::commit(&tail->finish);  // arrives once this thread's MMAs have all completed
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&tail->empty[s]);
-  }
-
-  if (timed_out) {
-    // Tell the other warps to stop, release them from the two merge barriers,
-    // and let copies already in flight land before the CTA's shared memory
-    // goes away.
+    // free tensor memory once every role is done with it
+    (void)mbar_wait(&tail->finish, 0);
+    tc::fence_after_thread_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  } else if (warp == 2) {
+    // ---- O^T = V^T P^T ----------------------------------------------------------------------
     if (lane == 0) {
-      *reinterpret_cast<volatile int*>(&tail->abort) = 1;
-      __threadfence_block();
-      mbar_arrive(&tail->drained);
-      mbar_arrive(&tail->merged);
+      const uint64_t a0 = tc::sw128_mnmajor_desc(smem_u32(smem + kHalfTile));
+      // B: N = 32 (16 hi heads, then 16 lo heads 128 bytes further); core
+      // matrices along K every kPBlock bytes.  Both offsets stay inside the
+      // 4 KiB buffer whichever of them strides along K.
+      const uint64_t b0 = tc::interleave_mnmajor_desc(smem_u32(pbuf), kPBlock, 128);
+      constexpr uint32_t idesc = tc::idesc_e4m3_f32_mn(128, 2 * kGroup);
+      for (int t = 0; t < n_pages; ++t) {
+        const int s = t % kStages, buf = t & 1;
+        if (!mbar_wait(&tail->p_full[buf], (t >> 1) & 1) ||
+            (t >= 2 && !mbar_wait(&tail->o_empty[buf], ((t >> 1) - 1) & 1))) {
+          flag_error(p.err, MSA_ERR_TIMEOUT);
+          break;
+        }
+        tc::fence_after_thread_sync();
+        // k-step kk = keys 32kk .. +31: 4 KiB into the V tile, 1 KiB into P^T
+        const uint64_t a = a0 + static_cast<uint64_t>(s) * (kStageBytes >> 4);
+        const uint64_t bp = b0 + static_cast<uint64_t>((2 * buf * kPPart) >> 4);
+        const uint32_t d = tmem + kColO + 2 * kGroup * buf;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3(d, a + 256 * kk, bp + 64 * kk, idesc, kk > 0);
+        tc::commit(&tail->o_full[buf]);
+        tc::commit(&tail->empty[s]);
+      }
+      tc::commit(&tail->finish);
     }
-    for (int t = consumed; t < n_pages && t < consumed + NST; ++t)
-      (void)mbar_wait(&tail->full[t % NST], (t / NST) & 1);
-    return;
-  }
-
-  // ---- merge the four warps' states ------------------------------------------
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  // every warp must be done reading the stages before they are reused
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&tail->drained);
-  if (!mbar_wait(&tail->drained, 0)) {
-    if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
-    return;
-  }
-  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
-  float* s_o = reinterpret_cast<float*>(smem);                   // [4][16][128]
-  float* s_m = s_o + kComputeWarps * kGroup * kHeadDim;          // [4][16]
-  float* s_l = s_m + kComputeWarps * kGroup;                     // [4][16]
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    float4 lo0, hi0, lo1, hi1;  // rows gr and gr+8, d = 32q4 + 8c + (0..3 | 4..7)
-    lo0 = make_float4(o[4 * q4 + 0][0], o[4 * q4 + 1][0], o[4 * q4 + 2][0], o[4 * q4 + 3][0]);
-    hi0 = make_float4(o[4 * q4 + 0][1], o[4 * q4 + 1][1], o[4 * q4 + 2][1], o[4 * q4 + 3][1]);
-    lo1 = make_float4(o[4 * q4 + 0][2], o[4 * q4 + 1][2], o[4 * q4 + 2][2], o[4 * q4 + 3][2]);
-    hi1 = make_float4(o[4 * q4 + 0][3], o[4 * q4 + 1][3], o[4 * q4 + 2][3], o[4 * q4 + 3][3]);
-    float* d0 = s_o + (warp * kGroup + gr) * kHeadDim + 32 * q4 + 8 * c;
-    float* d1 = d0 + 8 * kHeadDim;
-    *reinterpret_cast<float4*>(d0) = lo0;
-    *reinterpret_cast<float4*>(d0 + 4) = hi0;
-    *reinterpret_cast<float4*>(d1) = lo1;
-    *reinterpret_cast<float4*>(d1 + 4) = hi1;
-  }
-  if (c == 0) {
-    s_m[warp * kGroup + gr] = m0;
-    s_m[warp * kGroup + gr + 8] = m1;
-    s_l[warp * kGroup + gr] = l0;
-    s_l[warp * kGroup + gr + 8] = l1;
-  }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&tail->merged);
-  if (!mbar_wait(&tail->merged, 0)) {
-    if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
-    return;
-  }
-  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
-
-  // 128 threads: row r = tid / 8, 16 consecutive d per thread
-  const int tid = threadIdx.x;
-  const int r = tid >> 3, d0 = (tid & 7) * 16;
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, s_m[w * kGroup + r]);
-  float wt[kComputeWarps];
-  float Lsum = 0.f;
-#pragma unroll
-  for (int w = 0; w < kComputeWarps; ++w) {
-    const float mw = s_m[w * kGroup + r];
-    wt[w] = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-    Lsum += wt[w] * s_l[w * kGroup + r];
-  }
-  float acc_o[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) acc_o[e] = 0.f;
-#pragma unroll
-  for (int w = 0; w < kComputeWarps; ++w) {
-    const float* src = s_o + (w * kGroup + r) * kHeadDim + d0;
-#pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src + e);
-      acc_o[e] += wt[w] * v.x;
-      acc_o[e + 1] += wt[w] * v.y;
-      acc_o[e + 2] += wt[w] * v.z;
-      acc_o[e + 3] += wt[w] * v.w;
-    }
-  }
-  const int h = g * kGroup + r;
-  const int64_t row_idx = static_cast<int64_t>(i) * p.Hq + h;
-  if (p.splits == 1) {
-    const float f = (Lsum > 0.f) ? p.v_scale / Lsum : 0.f;
-    uint32_t packed[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      packed[e] = f32_to_bf16_bits(acc_o[2 * e] * f) | (f32_to_bf16_bits(acc_o[2 * e + 1] * f) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(p.out + row_idx * kHeadDim + d0);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   } else {
-    const int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hq;
-    float* dst = p.part_o + (static_cast<int64_t>(split) * rows + row_idx) * kHeadDim + d0;
+    // ---- softmax and output ------------------------------------------------------------------
+    const int quarter = warp & 3;
+    const int key = 32 * quarter + lane;  // key of the page; value dim d in the O^T phase
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+    const float zs = tail->zs;
+    // nref = kPShift - m, m the reference maximum of a head in log2 units
+    // (+inf until the head has seen a key); l: this key slot's share of the
+    // running sum; o: the running output of value dim `key`.  Both are kept
+    // relative to the current m.
+    float nref[kGroup], l[kGroup], o[kGroup];
+    fill(nref, INFINITY);
+    fill(l, 0.f);
+    fill(o, 0.f);
+    bool ok = true;
+
+    // o += f * O^T of page u (hi + lo columns), once its product is complete
+    auto add_page_o = [&](int u, const float (&f)[kGroup]) -> bool {
+      const int ob = u & 1;
+      if (!mbar_wait(&tail->o_full[ob], (u >> 1) & 1)) return false;
+      tc::fence_after_thread_sync();
+      uint32_t ov[32];
+      tc::ld_32x32b_x32(lane_addr + kColO + 2 * kGroup * ob, ov);
+      tc::wait_ld();
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->o_empty[ob]);
 #pragma unroll
-    for (int e = 0; e < 16; e += 4)
-      *reinterpret_cast<float4*>(dst + e) =
-          make_float4(acc_o[e] * p.v_scale, acc_o[e + 1] * p.v_scale, acc_o[e + 2] * p.v_scale,
-                      acc_o[e + 3] * p.v_scale);
-    if ((tid & 7) == 0) {
-      float* ml = p.part_ml + (static_cast<int64_t>(split) * rows + row_idx) * 2;
-      ml[0] = M;
-      ml[1] = Lsum;
+      for (int h = 0; h < kGroup; ++h)
+        o[h] = fmaf(__uint_as_float(ov[h]) + __uint_as_float(ov[h + kGroup]), f[h], o[h]);
+      return true;
+    };
+
+    for (int t = 0; t < n_pages && ok; ++t) {
+      const int buf = t & 1, ph = (t >> 1) & 1;
+      if (!mbar_wait(&tail->s_full[buf], ph)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_thread_sync();
+      float x[kGroup], pm[kGroup];
+      {
+        uint32_t sv[32];
+        tc::ld_32x32b_x32(lane_addr + kColS + 2 * kGroup * buf, sv);
+        tc::wait_ld();
+        tc::fence_before_thread_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->s_empty[buf]);
+        const int lim = pos - tail->blocks[t] * kPage;  // keys <= lim are visible
+        const bool vis = key <= lim;
+        // raw dot products (hi + lo columns); the logit in log2 units is
+        // s * zs with zs > 0, so maxima can be taken on s
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h)
+          x[h] = vis ? __uint_as_float(sv[h]) + __uint_as_float(sv[h + kGroup]) : -INFINITY;
+      }
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) pm[h] = warp_max_f32(x[h]);
+      float* mxb = mx + buf * 4 * kGroup;
+      if (lane == 0) {
+#pragma unroll
+        for (int h4 = 0; h4 < 4; ++h4)
+          *reinterpret_cast<float4*>(mxb + quarter * kGroup + 4 * h4) =
+              make_float4(pm[4 * h4], pm[4 * h4 + 1], pm[4 * h4 + 2], pm[4 * h4 + 3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->mx_full[buf]);
+      if (!mbar_wait(&tail->mx_full[buf], ph)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int h4 = 0; h4 < 4; ++h4) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(mxb + w * kGroup + 4 * h4);
+          pm[4 * h4] = fmaxf(pm[4 * h4], v.x);
+          pm[4 * h4 + 1] = fmaxf(pm[4 * h4 + 1], v.y);
+          pm[4 * h4 + 2] = fmaxf(pm[4 * h4 + 2], v.z);
+          pm[4 * h4 + 3] = fmaxf(pm[4 * h4 + 3], v.w);
+        }
+      }
+      // page maximum in log2 units against m + kLazy (pm + nref > kPShift + kLazy;
+      // a head without any key so far has nref = +inf and always moves)
+      bool raise = false;
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        pm[h] *= zs;
+        raise |= pm[h] + nref[h] > kPShift + kLazy;
+      }
+      float al[kGroup];  // 2^(m_old - m_new) per head
+      fill(al, 1.f);
+      if (raise) {  // the same decision in every thread
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          if (pm[h] + nref[h] > kPShift + kLazy) {
+            al[h] = ex2(kPShift - nref[h] - pm[h]);  // 0 when the head had no key yet
+            nref[h] = kPShift - pm[h];
+          }
+          o[h] *= al[h];
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        x[h] = ex2(fmaf(x[h], zs, nref[h]));  // P = 2^(x - m + 8); 0 for an invisible key
+        l[h] = fmaf(l[h], al[h], x[h]);
+      }
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t h0, l0, h1, l1;
+        split_e4m3x2(x[4 * q4], x[4 * q4 + 1], h0, l0);
+        split_e4m3x2(x[4 * q4 + 2], x[4 * q4 + 3], h1, l1);
+        hw[q4] = h0 | (h1 << 16);
+        lw[q4] = l0 | (l1 << 16);
+      }
+      const int s = t % kStages;
+      const int lim = pos - tail->blocks[t] * kPage;
+      if (lim < kPage - 1 && key > lim) {
+        // keys past the causal limit have P = 0, but their value rows may hold
+        // any bytes (an fp8 NaN times 0 is NaN): zero them for the O^T product
+        if (mbar_wait(&tail->full[s], (t / kStages) & 1)) {
+          uint4* vrow = reinterpret_cast<uint4*>(smem + s * kStageBytes + kHalfTile + key * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P^T: key k's 16 hi bytes at (k/8) * kPBlock + (k%8) * 16, its lo bytes
+      // 128 further (MN-major, no swizzle).  Buffer `buf` was last read by the
+      // O^T product of page t-2, which add_page_o(t-2) has waited for.
+      uint8_t* pk = pbuf + 2 * buf * kPPart + (key >> 3) * kPBlock + (key & 7) * 16;
+      *reinterpret_cast<uint4*>(pk) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(pk + 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->p_full[buf]);
+      // o holds pages <= t-2 relative to the new m; page t-1's product is
+      // relative to the previous m, so it enters with this page's factors
+      if (t >= 1 && !add_page_o(t - 1, al)) {
+        ok = false;
+        break;
+      }
     }
+    if (ok && n_pages > 0) {
+      float one[kGroup];
+      fill(one, 1.f);
+      ok = add_page_o(n_pages - 1, one);
+    }
+
+    if (ok) {
+      // running sums: this thread's share -> the whole page (128 key slots)
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h4 = 0; h4 < 4; ++h4)
+          *reinterpret_cast<float4*>(lsum + quarter * kGroup + 4 * h4) =
+              make_float4(l[4 * h4], l[4 * h4 + 1], l[4 * h4 + 2], l[4 * h4 + 3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->l_full);
+      ok = mbar_wait(&tail->l_full, 0);
+    }
+    if (ok) {
+#pragma unroll
+      for (int h4 = 0; h4 < 4; ++h4) {
+        float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(lsum + w * kGroup + 4 * h4);
+          t4.x += v.x;
+          t4.y += v.y;
+          t4.z += v.z;
+          t4.w += v.w;
+        }
+        l[4 * h4] = t4.x;
+        l[4 * h4 + 1] = t4.y;
+        l[4 * h4 + 2] = t4.z;
+        l[4 * h4 + 3] = t4.w;
+      }
+      const int d = key;
+      const int64_t row0 = static_cast<int64_t>(i) * p.Hq + g * kGroup;
+      if (p.splits == 1) {
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          const float f = (l[h] > 0.f) ? p.v_scale / l[h] : 0.f;
+          p.out[(row0 + h) * kHeadDim + d] = static_cast<uint16_t>(f32_to_bf16_bits(o[h] * f));
+        }
+      } else {
+        const int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hq;
+        const int64_t base = static_cast<int64_t>(split) * rows + row0;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) p.part_o[(base + h) * kHeadDim + d] = o[h] * p.v_scale;
+        // partial state in the combine kernel's terms: l = sum 2^(x - mref)
+        if (key < kGroup) {
+          float mr = -INFINITY, lr = 0.f;
+#pragma unroll
+          for (int h = 0; h < kGroup; ++h)
+            if (h == key) {
+              mr = -nref[h];  // m - kPShift; -inf for a head without keys
+              lr = l[h];
+            }
+          p.part_ml[(base + key) * 2] = mr;
+          p.part_ml[(base + key) * 2 + 1] = lr;
+        }
+      }
+    } else if (lane == 0) {
+      flag_error(p.err, MSA_ERR_TIMEOUT);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->finish);
   }
 }
 
@@ -443,26 +520,24 @@ __global__ void __launch_bounds__(256)
   *reinterpret_cast<uint2*>(out + r * kHeadDim + 4 * lane) = make_uint2(lo, hi);
 }
 
-constexpr int kAttendStages = 3;
 
 }  // namespace
 
 cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream) {
-  constexpr int smem = attend_smem_bytes<kAttendStages>();
-  static_assert(smem <= 227 * 1024, "attend shared memory");
+  static_assert(kSmemBytes <= 227 * 1024, "attend shared memory");
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    cudaError_t r = cudaFuncSetAttribute(attend_kernel<kAttendStages>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t r = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
     if (r != cudaSuccess) return r;
-    return cudaFuncSetAttribute(attend_kernel<kAttendStages>,
-                                cudaFuncAttributePreferredSharedMemoryCarveout,
+    // all of the unified L1 / shared storage as shared memory: two CTAs per SM
+    return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
   });
   if (e != cudaSuccess) return e;
   const int T = p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
-  attend_kernel<kAttendStages><<<grid, kThreads, smem, stream>>>(kv_map, p);
+  attend_kernel<<<grid, kThreads, kSmemBytes, stream>>>(kv_map, p);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
 // msa_device.cuh -- device helpers of the sm_103a sparse-decode kernels:
-// inline PTX for mbarriers, TMA tile loads, the m16n8k16 fp16 tensor-core MMA,
-// fp8 -> fp16 widening, and the fp16 query-row preparation.
+// inline PTX for mbarriers and TMA tile loads, fp8 conversions, warp
+// reductions, and the preparation of fp8 query tiles for the tensor core.
 #pragma once
 
 #include <cuda.h>
@@ -169,41 +169,8 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-// Power-of-two exponent e for a query row with largest magnitude `amax`, such
-// that amax * 2^-e lies in [2^14, 2^15): the row then rounds to fp16 with every
-// element >= amax * 2^-28 exact (bf16 has 8 significant bits).
-__device__ __forceinline__ int row_exponent(float amax) {
-  const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
-  if (biased == 0 || biased == 0xFF) return 0;  // zero/subnormal or non-finite row
-  int e = biased - 127 - 14;
-  return e < -100 ? -100 : (e > 100 ? 100 : e);
-}
-
 __device__ __forceinline__ float exp2i(int e) {  // 2^e for |e| <= 126
   return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-}
-
-// m16n8k16 tensor-core MMA, fp16 inputs, fp32 accumulate (in place).
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// m16n8k32 tensor-core MMA, fp8 e4m3 inputs, fp32 accumulate (in place).
-// A (16 x 32, row): a0/a2 = row lane/4, k 4(lane%4)..+3 and 16 + that; a1/a3
-// the same for row lane/4 + 8.  B (32 x 8, col): b0/b1 = k 4(lane%4)..+3 and
-// 16 + that, column lane/4.
-__device__ __forceinline__ void mma_e4m3_k32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                             uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Four floats -> four e4m3 bytes (x0 in the low byte).
@@ -211,9 +178,10 @@ __device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float x0, float x1, float x2
   return f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
 }
 
-// Exact split of four floats (each with at most 8 significant bits and a
-// magnitude below 2^8) into fp8 e4m3 hi + lo words with hi + lo == x for
-// every element whose magnitude is at least 2^-2.
+// Split of four floats (magnitude at most 448) into fp8 e4m3 hi + lo words:
+// hi = x rounded to e4m3, lo = (x - hi) rounded to e4m3, so hi + lo carries
+// about 8 significant bits of x, and is exact for a value with at most 8
+// significant bits and magnitude in [2^-2, 2^8).
 __device__ __forceinline__ void split_e4m3x4(const float (&x)[4], uint32_t& hi, uint32_t& lo) {
   const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
   uint32_t w01 = e4m3x2_to_f16x2(h01), w23 = e4m3x2_to_f16x2(h23);
@@ -224,140 +192,84 @@ __device__ __forceinline__ void split_e4m3x4(const float (&x)[4], uint32_t& hi, 
                        x[2] - __low2float(f23), x[3] - __high2float(f23));
 }
 
-// Query fragments for the fp8 QK^T MMA (m16n8k32): the 16 query heads of one
-// (token, KV head), scaled by a per-token power of two 2^-e so that the
-// largest element lies in [2^7, 2^8), then split exactly into e4m3 hi + lo.
-// Lane (gr = lane/4, c = lane%4) gets, for k-step ks (d = 32ks .. 32ks+31):
-//   hi/lo[0] = row gr,   d 32ks + 4c .. +3      hi/lo[2] = row gr,   d +16
-//   hi/lo[1] = row gr+8, d 32ks + 4c .. +3      hi/lo[3] = row gr+8, d +16
-// Only k-step `ks_only` (0..3) is split and returned; the exponent e always
-// comes from the whole token.  `mul` receives scale * 2^e.
-__device__ __forceinline__ void load_query_fragments_e4m3(const uint16_t* __restrict__ q_rows,
-                                                          int lane, float scale, int ks_only,
-                                                          uint32_t (&hi)[4], uint32_t (&lo)[4],
-                                                          float& mul) {
-  const int gr = lane >> 2, c = lane & 3;
-  uint2 raw[4][4];  // [ks][fragment register]
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-      const int row = gr + 8 * (f & 1), d = 32 * ks + 16 * (f >> 1) + 4 * c;
-      raw[ks][f] = __ldg(reinterpret_cast<const uint2*>(q_rows + row * kHeadDim + d));
-    }
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].x & 0xFFFF)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].x >> 16)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].y & 0xFFFF)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(raw[ks][f].y >> 16)));
-    }
-  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
-  const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
-  int e = (biased == 0 || biased == 0xFF) ? 0 : biased - 127 - 7;
-  e = e < -100 ? -100 : (e > 100 ? 100 : e);
-  const float sd = exp2i(-e);
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    if (ks != ks_only) continue;
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-      const float x[4] = {bf16_bits_to_f32(raw[ks][f].x & 0xFFFF) * sd,
-                          bf16_bits_to_f32(raw[ks][f].x >> 16) * sd,
-                          bf16_bits_to_f32(raw[ks][f].y & 0xFFFF) * sd,
-                          bf16_bits_to_f32(raw[ks][f].y >> 16) * sd};
-      split_e4m3x4(x, hi[f], lo[f]);
-    }
-  }
-  mul = scale * exp2i(e);
-}
-
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// ----------------------------------------------------------------------------
-// Query fragments.
-//
-// The 128-wide head dimension is permuted inside every 16-wide k-step of the
-// MMA so that each lane's four k values are four consecutive bytes of a cached
-// fp8 key row: logical k (2c, 2c+1, 2c+8, 2c+9) of k-step ks <-> physical d
-// (16ks + 4c .. 16ks + 4c + 3).  The same permutation is applied to q, so the
-// dot products are unchanged.  Lane (gr = lane/4, c = lane%4) of a warp holds,
-// for the 16 query heads of one (token, KV head), A-fragment registers
-//   a[ks][0] = q[gr  ][16ks+4c .. +1]   a[ks][2] = q[gr  ][16ks+4c+2 .. +3]
-//   a[ks][1] = q[gr+8][16ks+4c .. +1]   a[ks][3] = q[gr+8][16ks+4c+2 .. +3]
-// as fp16 after scaling row r by 2^-e_r.  `mul0/mul1` receive
-// `scale * 2^e_r` for rows gr and gr+8.
-__device__ __forceinline__ void load_query_fragments(const uint16_t* __restrict__ q_rows,
-                                                     int lane, float scale, uint32_t (&a)[8][4],
-                                                     float& mul0, float& mul1) {
-  const int gr = lane >> 2, c = lane & 3;
-  const uint16_t* r0 = q_rows + gr * kHeadDim + 4 * c;
-  const uint16_t* r1 = r0 + 8 * kHeadDim;
-  uint2 raw0[8], raw1[8];
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    raw0[ks] = __ldg(reinterpret_cast<const uint2*>(r0 + 16 * ks));
-    raw1[ks] = __ldg(reinterpret_cast<const uint2*>(r1 + 16 * ks));
-  }
-  float amax0 = 0.f, amax1 = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    amax0 = fmaxf(amax0, fabsf(bf16_bits_to_f32(raw0[ks].x & 0xFFFF)));
-    amax0 = fmaxf(amax0, fabsf(bf16_bits_to_f32(raw0[ks].x >> 16)));
-    amax0 = fmaxf(amax0, fabsf(bf16_bits_to_f32(raw0[ks].y & 0xFFFF)));
-    amax0 = fmaxf(amax0, fabsf(bf16_bits_to_f32(raw0[ks].y >> 16)));
-    amax1 = fmaxf(amax1, fabsf(bf16_bits_to_f32(raw1[ks].x & 0xFFFF)));
-    amax1 = fmaxf(amax1, fabsf(bf16_bits_to_f32(raw1[ks].x >> 16)));
-    amax1 = fmaxf(amax1, fabsf(bf16_bits_to_f32(raw1[ks].y & 0xFFFF)));
-    amax1 = fmaxf(amax1, fabsf(bf16_bits_to_f32(raw1[ks].y >> 16)));
-  }
-  amax0 = fmaxf(amax0, __shfl_xor_sync(0xffffffffu, amax0, 1));
-  amax0 = fmaxf(amax0, __shfl_xor_sync(0xffffffffu, amax0, 2));
-  amax1 = fmaxf(amax1, __shfl_xor_sync(0xffffffffu, amax1, 1));
-  amax1 = fmaxf(amax1, __shfl_xor_sync(0xffffffffu, amax1, 2));
-  const int e0 = row_exponent(amax0), e1 = row_exponent(amax1);
-  const float s0 = exp2i(-e0), s1 = exp2i(-e1);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    a[ks][0] = pack_f16x2(bf16_bits_to_f32(raw0[ks].x & 0xFFFF) * s0,
-                          bf16_bits_to_f32(raw0[ks].x >> 16) * s0);
-    a[ks][2] = pack_f16x2(bf16_bits_to_f32(raw0[ks].y & 0xFFFF) * s0,
-                          bf16_bits_to_f32(raw0[ks].y >> 16) * s0);
-    a[ks][1] = pack_f16x2(bf16_bits_to_f32(raw1[ks].x & 0xFFFF) * s1,
-                          bf16_bits_to_f32(raw1[ks].x >> 16) * s1);
-    a[ks][3] = pack_f16x2(bf16_bits_to_f32(raw1[ks].y & 0xFFFF) * s1,
-                          bf16_bits_to_f32(raw1[ks].y >> 16) * s1);
-  }
-  mul0 = scale * exp2i(e0);
-  mul1 = scale * exp2i(e1);
+// Two non-negative floats (at most 448) -> fp8 e4m3 hi and lo pairs (x0 in
+// the low byte): hi = x rounded to e4m3 (through fp16), lo = the remainder
+// rounded to e4m3; hi + lo carries about 8 significant bits of x.
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  uint16_t h8, l8;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(*reinterpret_cast<const uint32_t*>(&h)));
+  const uint32_t hb = e4m3x2_to_f16x2(h8);
+  const __half2 r = __hsub2(h, *reinterpret_cast<const __half2*>(&hb));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(*reinterpret_cast<const uint32_t*>(&r)));
+  hi = h8;
+  lo = l8;
 }
 
-// S = Q K^T for one warp: the 16 query heads of `a` against 32 keys
-// (rows key0 .. key0+31) of a swizzled K half-page tile.  acc[tile][0..1] are
-// row gr, keys key0 + 8*tile + 2c + {0,1}; acc[tile][2..3] row gr+8.
-__device__ __forceinline__ void qk_32keys(const uint8_t* __restrict__ ktile, int key0, int lane,
-                                          const uint32_t (&a)[8][4], float (&acc)[4][4]) {
-  const int gr = lane >> 2, c = lane & 3;
+// Largest of a float across the warp (every lane gets it); NaN inputs are
+// ignored unless every lane holds one.
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// ----------------------------------------------------------------------------
+// Query tiles for the fp8 tensor-core products.
+//
+// The 16 query rows of one (token, KV head) (bf16, 16 x 128, row stride 128)
+// are scaled by a power of two 2^-e, e chosen so that the largest magnitude
+// of the 16 rows lies in [2^7, 2^8), and split into fp8 e4m3 hi + lo parts
+// (bf16's 8 significant bits are 4 + 4, so hi + lo equals the scaled value for
+// every element of magnitude >= 2^-2, i.e. all but those 2^9 times smaller
+// than the largest).  The parts are written as rows row0 .. row0+15 of two
+// K-major tiles with 128-byte rows and 128-byte swizzling.  One warp (lane:
+// row lane/2, d 64*(lane&1) .. +63); returns e, the same in every lane.
+__device__ __forceinline__ int prepare_query_e4m3(const uint16_t* __restrict__ rows, int row0,
+                                                  uint8_t* hi, uint8_t* lo, int lane) {
+  const int r = lane >> 1, half = lane & 1;
+  const uint4* src = reinterpret_cast<const uint4*>(rows + r * kHeadDim + 64 * half);
+  uint4 raw[8];
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
+  for (int k = 0; k < 8; ++k) raw[k] = __ldg(src + k);
+  float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int row = key0 + 8 * t + gr;
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(ktile + sw128(row, ks) + 4 * c);
-      mma_f16(acc[t], a[ks], e4m3x2_to_f16x2(w & 0xFFFF), e4m3x2_to_f16x2(w >> 16));
+    for (int e = 0; e < 4; ++e) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] & 0xFFFF)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] >> 16)));
     }
   }
+  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+  const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  int e = (biased == 0 || biased == 0xFF) ? 0 : biased - 127 - 7;  // amax*2^-e in [2^7, 2^8)
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  const float sd = exp2i(-e);
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const int el = 16 * c4 + 4 * wi;  // elements el .. el+3 of this lane's 64
+      const uint4 v = raw[el >> 3];
+      const uint32_t pair0 = ((el & 7) == 0) ? v.x : v.z;
+      const uint32_t pair1 = ((el & 7) == 0) ? v.y : v.w;
+      const float x[4] = {bf16_bits_to_f32(pair0 & 0xFFFF) * sd, bf16_bits_to_f32(pair0 >> 16) * sd,
+                          bf16_bits_to_f32(pair1 & 0xFFFF) * sd, bf16_bits_to_f32(pair1 >> 16) * sd};
+      split_e4m3x4(x, hw[wi], lw[wi]);
+    }
+    const int off = sw128(row0 + r, 4 * half + c4);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  return e;
 }
 
 }  // namespace msa

@@ -170,50 +170,9 @@ __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk&
 // swizzled, K-major), per-token factors scale * 2^e into qmul[0..Q).
 __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
                                    float* qmul, int lane) {
-  const int Q = p.Q;
-  for (int jq = 0; jq < Q; ++jq) {
-    const int r = lane >> 1, half = lane & 1;
-    const uint16_t* src =
-        p.q + ((static_cast<int64_t>(b) * Q + jq) * p.Hq + g * kGroup + r) * kHeadDim + 64 * half;
-    uint4 raw[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) raw[k] = __ldg(reinterpret_cast<const uint4*>(src) + k);
-    float amax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] & 0xFFFF)));
-        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] >> 16)));
-      }
-    }
-    amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
-    const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
-    int e = (biased == 0 || biased == 0xFF) ? 0 : biased - 127 - 7;  // amax*2^-e in [2^7, 2^8)
-    e = e < -100 ? -100 : (e > 100 ? 100 : e);
-    const float sd = exp2i(-e);
-    const int R = jq * kGroup + r;
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        // elements 16*c4 + 4*wi .. +3 of this lane's 64
-        const int el = 16 * c4 + 4 * wi;
-        const uint4 v = raw[el >> 3];
-        const uint32_t pair0 = ((el & 7) == 0) ? v.x : v.z;
-        const uint32_t pair1 = ((el & 7) == 0) ? v.y : v.w;
-        const float x[4] = {bf16_bits_to_f32(pair0 & 0xFFFF) * sd,
-                            bf16_bits_to_f32(pair0 >> 16) * sd,
-                            bf16_bits_to_f32(pair1 & 0xFFFF) * sd,
-                            bf16_bits_to_f32(pair1 >> 16) * sd};
-        split_e4m3x4(x, hw[wi], lw[wi]);
-      }
-      const int off = sw128(R, 4 * half + c4);
-      *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
+  for (int jq = 0; jq < p.Q; ++jq) {
+    const uint16_t* rows = p.q + ((static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup) * kHeadDim;
+    const int e = prepare_query_e4m3(rows, jq * kGroup, qhi, qlo, lane);
     if (lane == 0) qmul[jq] = p.scale * exp2i(e);
   }
 }
