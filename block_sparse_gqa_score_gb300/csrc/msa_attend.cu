@@ -111,13 +111,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) {
     // this CTA's page list, barriers, and the first loads
     const int L = p.seq_lens[b];
+    pdl_wait();  // the top-k lists come from the previous kernel
+    int n = lane < kTopK ? p.topk[(static_cast<int64_t>(i) * p.Hkv + g) * kTopK + lane] : -1;
     const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
     const int pos = seq_ok ? L - p.Q + j : -1;
-    int n = -1, page = -1;
+    int page = -1;
     bool valid = false;
     if (lane < kTopK && pos >= 0) {
-      n = p.topk[(static_cast<int64_t>(i) * p.Hkv + g) * kTopK + lane];
       if (n != -1) {
         if (n < 0 || n > pos / kPage)
           flag_error(p.err, MSA_ERR_TOPK_RANGE);
@@ -209,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(st + kHalfTile, &kv_map, kHeadDim, row, &tail->full[s]);
         issued = t + 1;
       }
+      // every load of this CTA is issued: the next kernel may start its CTAs
+      pdl_trigger();
       // the loads still in flight land before shared memory can be released
       for (int t = issued - kStages; t < issued; ++t)
         if (t >= 0) (void)mbar_wait(&tail->full[t % kStages], (t / kStages) & 1);
@@ -491,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                    uint16_t* __restrict__ out, int64_t rows, int splits) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the attend kernel
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -537,8 +542,7 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   if (e != cudaSuccess) return e;
   const int T = p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
-  attend_kernel<<<grid, kThreads, kSmemBytes, stream>>>(kv_map, p);
-  return cudaGetLastError();
+  return launch_pdl(attend_kernel, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
@@ -546,9 +550,8 @@ cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* 
   const int64_t threads = rows * 32;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
-  combine_kernel<<<static_cast<unsigned>(grid), block, 0, stream>>>(part_o, part_ml, out, rows,
-                                                                   splits);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(block), 0, stream,
+                    part_o, part_ml, out, rows, splits);
 }
 
 }  // namespace msa

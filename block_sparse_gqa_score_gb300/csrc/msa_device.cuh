@@ -44,6 +44,24 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch
+//
+// pdl_trigger: this CTA lets the next kernel on the stream (launched with the
+// programmatic stream serialization attribute) schedule its CTAs once every
+// CTA of this grid has triggered or exited, so that their prologue overlaps
+// this kernel's tail (the streaming kernels trigger after their last load).  pdl_wait: the calling thread
+// waits until the previous kernel on the stream has completed and its memory
+// writes are visible (at once when this launch overlapped no kernel).  Each
+// kernel calls pdl_wait before its first read of a previous kernel's output
+// and before its first write of anything a previous kernel may still read.
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
 // mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {

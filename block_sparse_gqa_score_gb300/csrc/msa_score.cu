@@ -313,6 +313,9 @@ __global__ void __maxnreg__(128)
                     &tail->full[s]);
         ++vp;
       }
+      // every load of this CTA is issued: the next kernel may start its CTAs
+      // (its prologue then overlaps this kernel's last pages)
+      pdl_trigger();
       // the last loads in flight land before shared memory can be released
       for (int t = vp - G.stages; t < vp; ++t)
         if (t >= 0) (void)mbar_wait(&tail->full[t % G.stages], (t / G.stages) & 1);
@@ -415,7 +418,9 @@ __global__ void __maxnreg__(128)
       ++k;
     }
     // -inf for blocks past each request's last visible block (units dealt
-    // round-robin over the CTAs; disjoint from every page written above)
+    // round-robin over the CTAs; disjoint from every page written above);
+    // the previous kernel on the stream may still be reading scores
+    pdl_wait();
     for (int64_t u = blockIdx.x; u < static_cast<int64_t>(p.B) * p.Hkv; u += gridDim.x) {
       const int b = static_cast<int>(u / p.Hkv), g = static_cast<int>(u - static_cast<int64_t>(b) * p.Hkv);
       const int nhi = visible_blocks(p, b);
@@ -499,6 +504,7 @@ __global__ void __maxnreg__(128)
     if (lane == 0) mbar_arrive(&tail->finish);
   } else {
     // ---- combiner: four quarters -> scores ---------------------------------------------
+    pdl_wait();  // the first write of scores
     PageWalk w;
     if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
     int k = -1, pb = -1, pg = -1, vp = 0;
@@ -562,8 +568,8 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
   });
   if (e != cudaSuccess) return e;
-  score_kernel<<<p.ctas * G.per_sm, kThreads, G.smem, stream>>>(kv_map, p);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel, dim3(p.ctas * G.per_sm), dim3(kThreads), G.smem, stream, kv_map,
+                    p);
 }
 
 }  // namespace msa

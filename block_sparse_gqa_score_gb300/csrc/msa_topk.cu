@@ -64,6 +64,8 @@ __device__ __forceinline__ uint32_t tau_in_registers(LoadKey& load_key, uint32_t
 
 __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
   __shared__ uint32_t s_keys[kWarps][kCache];
+  pdl_trigger();
+  pdl_wait();  // scores come from the previous kernel; topk may still be read by one
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int T = p.B * p.Q;
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hkv;
   const int64_t grid = (rows + kWarps - 1) / kWarps;
-  topk_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kWarps * 32), 0, stream,
+                    p);
 }
 
 }  // namespace msa
