@@ -183,9 +183,9 @@ def _source_digest(*names) -> str:
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"attend": ("msa_attend.cu", "msa_device.cuh"),
-                  "score": ("msa_score.cu", "msa_device.cuh"),
-                  "topk": ("msa_topk.cu",)}
+KERNEL_SOURCES = {"attend": ("msa_attend.cu", "msa_device.cuh", "msa_tcgen05.cuh", "msa_launch.h"),
+                  "score": ("msa_score.cu", "msa_device.cuh", "msa_tcgen05.cuh", "msa_launch.h"),
+                  "topk": ("msa_topk.cu", "msa_device.cuh", "msa_launch.h")}
 
 
 def _traffic_from_profiles(stage: str, workload: str):
