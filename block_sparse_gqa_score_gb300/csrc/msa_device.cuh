@@ -247,14 +247,21 @@ __device__ __forceinline__ float warp_max_f32(float x) {
 // every element of magnitude >= 2^-2, i.e. all but those 2^9 times smaller
 // than the largest).  The parts are written as rows row0 .. row0+15 of two
 // K-major tiles with 128-byte rows and 128-byte swizzling.  One warp (lane:
-// row lane/2, d 64*(lane&1) .. +63); returns e, the same in every lane.
-__device__ __forceinline__ int prepare_query_e4m3(const uint16_t* __restrict__ rows, int row0,
-                                                  uint8_t* hi, uint8_t* lo, int lane) {
-  const int r = lane >> 1, half = lane & 1;
-  const uint4* src = reinterpret_cast<const uint4*>(rows + r * kHeadDim + 64 * half);
-  uint4 raw[8];
+// row lane/2, d 64*(lane&1) .. +63).
+
+// The lane's 64 bf16 values (global loads only; nothing waits on them yet).
+__device__ __forceinline__ void load_query_rows(const uint16_t* __restrict__ rows, int lane,
+                                                uint4 (&raw)[8]) {
+  const uint4* src = reinterpret_cast<const uint4*>(rows + (lane >> 1) * kHeadDim + 64 * (lane & 1));
 #pragma unroll
   for (int k = 0; k < 8; ++k) raw[k] = __ldg(src + k);
+}
+
+// Scale, split and store the values load_query_rows fetched; returns e (the
+// same in every lane).
+__device__ __forceinline__ int store_query_e4m3(const uint4 (&raw)[8], int row0, uint8_t* hi,
+                                                uint8_t* lo, int lane) {
+  const int r = lane >> 1, half = lane & 1;
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -288,6 +295,13 @@ __device__ __forceinline__ int prepare_query_e4m3(const uint16_t* __restrict__ r
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   return e;
+}
+
+__device__ __forceinline__ int prepare_query_e4m3(const uint16_t* __restrict__ rows, int row0,
+                                                  uint8_t* hi, uint8_t* lo, int lane) {
+  uint4 raw[8];
+  load_query_rows(rows, lane, raw);
+  return store_query_e4m3(raw, row0, hi, lo, lane);
 }
 
 }  // namespace msa
