@@ -8,12 +8,15 @@
 // scorer's [head, token, block] buffer through a transposed view.
 //
 // Design: one warp per row.  Scores become order-preserving 32-bit keys
-// (larger float -> larger key, -0 folded onto +0).  The 15th-largest key tau
-// is found by a bitwise binary search from the most significant bit: for each
-// bit, count (one compare per key, one warp-wide redux add) the keys at or
-// above the candidate prefix, and keep the bit when at least 15 are.  Keys
-// > tau are all kept and the lowest-index keys == tau fill the rest, in one
-// ordered sweep.  Rows of up to 512 candidates live in registers (16 per
+// (larger float -> larger key, -0 folded onto +0).  A threshold tau with at
+// least 15 keys >= tau is found by a bitwise binary search: for each bit,
+// count (one compare per key, one warp-wide redux add) the keys at or above
+// the candidate prefix, and keep the bit when at least 15 are.  The search
+// starts below the bits that the row's smallest and largest keys share (every
+// key shares them, so tau does too), and stops as soon as exactly 15 keys are
+// >= tau: they are then the kept set, with no tie at its boundary.  Without
+// an early stop tau ends as the 15th-largest key.  Keys > tau are all kept and
+// the lowest-index keys == tau fill the rest, in one ordered sweep.  Rows of up to 512 candidates live in registers (16 per
 // lane), rows up to kCache in shared memory, longer rows are re-read.
 #include "msa_device.cuh"
 #include "msa_launch.h"
@@ -48,13 +51,30 @@ __device__ __forceinline__ uint32_t tau_in_registers(LoadKey& load_key, uint32_t
     const int n = lane + 32 * e;
     kr[e] = (n < cur) ? load_key(n) : 0u;  // 0 ranks below every real key
   }
-  uint32_t tau = 0;
-  for (int bit = 31; bit >= 0; --bit) {
+  // bits above the highest one where the row's extreme keys differ are
+  // common to every key (absent slots hold 0, the smallest key, and take part)
+  uint32_t lo_k = 0xFFFFFFFFu, hi_k = 0u;
+#pragma unroll
+  for (int e = 0; e < NK; ++e) {
+    if (lane + 32 * e < cur) lo_k = min(lo_k, kr[e]);
+    hi_k = max(hi_k, kr[e]);
+  }
+  lo_k = __reduce_min_sync(0xffffffffu, lo_k);
+  hi_k = __reduce_max_sync(0xffffffffu, hi_k);
+  const uint32_t diff = lo_k ^ hi_k;
+  const int top = diff ? 31 - __clz(diff) : -1;       // highest differing bit
+  uint32_t tau = top >= 0 ? (hi_k & ~((2u << top) - 1u)) : hi_k;
+  if (top == 31) tau = 0;
+  for (int bit = top; bit >= 0; --bit) {
     const uint32_t cand = tau | (1u << bit);
     int cnt = 0;
 #pragma unroll
     for (int e = 0; e < NK; ++e) cnt += (kr[e] >= cand) ? 1 : 0;
-    if (__reduce_add_sync(0xffffffffu, cnt) >= kSel) tau = cand;
+    const int total = __reduce_add_sync(0xffffffffu, cnt);
+    if (total >= kSel) {
+      tau = cand;
+      if (total == kSel) break;  // exactly the 15 kept keys are >= tau
+    }
   }
 #pragma unroll
   for (int e = 0; e < NK; ++e)
