@@ -530,54 +530,107 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
     (q, seq_lens, block_table, and the given top-k for attend-only workloads)
     copied from pinned host memory and the output copied back to pinned host
     memory; the KV cache is resident model state.  The steps (copies and API
-    calls) are captured once into CUDA graphs, as a serving loop would, and the
-    graphs are replayed in the timed region; if capture fails the same calls
-    run eagerly."""
+    calls) are captured once into a CUDA graph, as a serving loop would, with
+    the copies double-buffered on a second stream, and the graph is replayed in
+    the timed region; if capture fails the same calls run eagerly."""
     n_layers = len(layers)
-    host = []
-    for inp in layers:
-        h = {"q": inp.q.cpu().pin_memory(), "seq_lens": inp.seq_lens.cpu().pin_memory(),
-             "block_table": inp.block_table.cpu().pin_memory()}
+    # each layer's step inputs packed in one pinned buffer (q, seq_lens,
+    # block_table[, top-k], each 256-byte aligned), copied with one transfer
+    # into a device buffer of the same layout that the API calls view
+
+    def layout(inp):
+        parts = [("q", inp.q), ("seq_lens", inp.seq_lens), ("block_table", inp.block_table)]
         if w.topk_given:
-            h["topk"] = inp.topk.cpu().pin_memory()
-        h["out"] = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        host.append(h)
-    dq = [torch.empty_like(inp.q) for inp in layers]
-    dsl = [torch.empty_like(inp.seq_lens) for inp in layers]
-    dbt = [torch.empty_like(inp.block_table) for inp in layers]
-    dtk = [torch.empty_like(inp.topk) if w.topk_given else None for inp in layers]
-    h2d = host[0]["q"].numel() * 2 + host[0]["seq_lens"].numel() * 4 + \
-        host[0]["block_table"].numel() * 4 + (host[0]["topk"].numel() * 4 if w.topk_given else 0)
-    d2h = host[0]["out"].numel() * 2
+            parts.append(("topk", inp.topk))
+        offs, off = {}, 0
+        for name, t in parts:
+            offs[name] = (off, t)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    host, dev_in, views = [], [], []
+    for inp in layers:
+        offs, nbytes = layout(inp)
+        hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        v = {}
+        for name, (off, t) in offs.items():
+            n = t.numel() * t.element_size()
+            hbuf[off:off + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            v[name] = dbuf[off:off + n].view(t.dtype).view(t.shape)
+        host.append({"in": hbuf, "out": torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()})
+        dev_in.append(dbuf)
+        views.append(v)
+    h2d_bytes = sum(t.numel() * t.element_size() for _, t in layout(layers[0])[0].values())
+    d2h_bytes = host[0]["out"].numel() * 2
     steps = min(args.steps, 500)
 
-    def one(k):
-        l = k % n_layers
-        inp, bf, h = layers[l], bufs[l], host[l]
-        dq[l].copy_(h["q"], non_blocking=True)
-        dsl[l].copy_(h["seq_lens"], non_blocking=True)
-        dbt[l].copy_(h["block_table"], non_blocking=True)
-        if w.topk_given:
-            dtk[l].copy_(h["topk"], non_blocking=True)
-            msa.sparse_decode(dq[l], inp.kv, dbt[l], dsl[l], dtk[l], inp.qlen, inp.sm_scale,
-                              inp.k_scale, inp.v_scale, out=bf.out, num_splits=bf.num_splits,
-                              workspace=bf.workspace)
-        else:
-            msa.decode_step(dq[l], inp.kv, dbt[l], dsl[l], inp.qlen, inp.sm_scale, inp.k_scale,
-                            inp.v_scale, buffers=bf)
-        h["out"].copy_(bf.out, non_blocking=True)
+    copy_stream = torch.cuda.Stream(dev)
 
-    mode = "public Python API captured in CUDA graphs (copies included)"
+    def h2d(k):
+        l = k % n_layers
+        dev_in[l].copy_(host[l]["in"], non_blocking=True)
+
+    def compute(k):
+        l = k % n_layers
+        inp, bf, v = layers[l], bufs[l], views[l]
+        if w.topk_given:
+            msa.sparse_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], v["topk"],
+                              inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
+                              num_splits=bf.num_splits, workspace=bf.workspace)
+        else:
+            msa.decode_step(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
+                            inp.sm_scale, inp.k_scale, inp.v_scale, buffers=bf)
+
+    def d2h(k):
+        l = k % n_layers
+        host[l]["out"].copy_(bufs[l].out, non_blocking=True)
+
+    out_stream = torch.cuda.Stream(dev)
+
+    def run(nsteps):
+        """Every step's copies and API calls.  Step k+1's inputs are copied on
+        one side stream while step k's kernels run, and step k's output is read
+        back on another; a layer's device buffers are reused only after the
+        step that last read or wrote them."""
+        done = [torch.cuda.Event() for _ in range(nsteps)]     # step k's kernels done
+        landed = [torch.cuda.Event() for _ in range(nsteps)]   # step k's inputs on the device
+        read = [torch.cuda.Event() for _ in range(nsteps)]     # step k's output read back
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_stream(stream)
+            h2d(0)
+            landed[0].record(copy_stream)
+        out_stream.wait_stream(stream)
+        for k in range(nsteps):
+            if k + 1 < nsteps:
+                with torch.cuda.stream(copy_stream):
+                    if k + 1 - n_layers >= 0:
+                        copy_stream.wait_event(done[k + 1 - n_layers])
+                    h2d(k + 1)
+                    landed[k + 1].record(copy_stream)
+            stream.wait_event(landed[k])
+            if k - n_layers >= 0:
+                stream.wait_event(read[k - n_layers])
+            with torch.cuda.stream(stream):
+                compute(k)
+            done[k].record(stream)
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(done[k])
+                d2h(k)
+                read[k].record(out_stream)
+        stream.wait_stream(copy_stream)
+        stream.wait_stream(out_stream)
+
+    mode = ("public Python API captured in a CUDA graph; each step's input copy and output "
+            "read-back on side streams, overlapping the neighbouring steps' kernels")
     graph = None
     with torch.cuda.stream(stream):
-        for k in range(min(args.warmup, 20)):
-            one(k)
+        run(min(args.warmup, 20) or 1)
         torch.cuda.synchronize(dev)
         try:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                for k in range(steps):
-                    one(k)
+                run(steps)
             graph.replay()                      # upload
             torch.cuda.synchronize(dev)
         except Exception as e:  # pragma: no cover - depends on the torch build
@@ -588,13 +641,12 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
         if graph is not None:
             graph.replay()
         else:
-            for k in range(steps):
-                one(k)
+            run(steps)
         b.record()
         torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b)
     return {"value": world * w.tokens * steps / (ms / 1e3), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
             "ms_per_step": ms / steps, "path": mode}
 
 
