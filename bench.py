@@ -5,8 +5,8 @@
                     [--workload NAME]
 
 Prints ONE JSON line.  A step is one pass of the whole decode step for one
-layer's batch: msa_score, msa_topk, msa_sparse_decode (+ msa_combine when
-split).  Inputs are synthetic and resident in HBM before the timed region; the
+layer's batch: msa_score, then msa_sparse_decode_select (the block selection
+and the attend in one kernel; + msa_combine when split).  Inputs are synthetic and resident in HBM before the timed region; the
 layers rotate over independent KV pools whose total size is >= 4x the L2, so
 no step finds its inputs in L2.  The timed region is a CUDA-graph replay of
 the K steps (kernels only), bracketed by CUDA events on the launch stream.
@@ -183,9 +183,10 @@ def _source_digest(*names) -> str:
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"attend": ("msa_attend.cu", "msa_device.cuh", "msa_tcgen05.cuh", "msa_launch.h"),
+KERNEL_SOURCES = {"attend": ("msa_attend.cu", "msa_device.cuh", "msa_tcgen05.cuh", "msa_launch.h",
+                             "msa_select.cuh"),
                   "score": ("msa_score.cu", "msa_device.cuh", "msa_tcgen05.cuh", "msa_launch.h"),
-                  "topk": ("msa_topk.cu", "msa_device.cuh", "msa_launch.h")}
+                  "topk": ("msa_topk.cu", "msa_device.cuh", "msa_launch.h", "msa_select.cuh")}
 
 
 def _traffic_from_profiles(stage: str, workload: str):
@@ -365,15 +366,17 @@ def run_ours(args, rank, world, local):
                                               inp.topk, inp.qlen, inp.sm_scale, inp.k_scale,
                                               inp.v_scale, out=bf.out, num_splits=bf.num_splits,
                                               workspace=bf.workspace)]
+        # the selection runs inside the attend kernel (msa_sparse_decode_select)
         return [lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
                                   inp.sm_scale, inp.k_scale, scores=bf.scores),
-                lambda: msa.topk(bf.scores, inp.seq_lens, inp.qlen, out=bf.topk),
-                lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk,
-                                          inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
-                                          out=bf.out, num_splits=bf.num_splits,
-                                          workspace=bf.workspace)]
+                lambda: None,
+                lambda: msa.sparse_decode_select(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                                 bf.scores, inp.qlen, inp.sm_scale, inp.k_scale,
+                                                 inp.v_scale, topk_out=bf.topk, out=bf.out,
+                                                 num_splits=bf.num_splits,
+                                                 workspace=bf.workspace)]
 
-    launches_per_step = (1 if w.topk_given else 3) + (1 if splits > 1 else 0)
+    launches_per_step = (1 if w.topk_given else 2) + (1 if splits > 1 else 0)
 
     # warm-up (eager), then the per-layer work figures from the real top-k lists
     msa.get_error(clear=True)
@@ -447,8 +450,8 @@ def run_ours(args, rank, world, local):
     avg_ms = {k: 0.0 for k in stage_names}
     reps_stage = min(args.steps, chunk)
     for s_i, k in enumerate(stage_names):
-        if w.topk_given and k != "attend":
-            continue
+        if k == "topk" or (w.topk_given and k != "attend"):
+            continue   # the selection is part of the attend kernel
         try:
             g = capture(reps_stage, which=(s_i,)) if graphs else None
         except Exception:  # pragma: no cover
@@ -467,18 +470,51 @@ def run_ours(args, rank, world, local):
             b.record(stream)
         b.synchronize()
         avg_ms[k] = _max_over_ranks(a.elapsed_time(b), world) / reps_stage
+    # the attend on its own (msa_sparse_decode over the lists the step selected),
+    # the kernel the gathered-KV figure is defined on
+    attend_alone_ms = avg_ms["attend"]
+    if not w.topk_given:
+        def plain(l):
+            inp, bf = layers[l], bufs[l]
+            msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk, inp.qlen,
+                              inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
+                              num_splits=bf.num_splits, workspace=bf.workspace)
+        g = None
+        if graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(reps_stage):
+                    plain(j % n_layers)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            if g is not None:
+                g.replay()
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            if g is not None:
+                g.replay()
+            else:
+                for j in range(reps_stage):
+                    plain(j % n_layers)
+            b.record(stream)
+        b.synchronize()
+        attend_alone_ms = _max_over_ranks(a.elapsed_time(b), world) / reps_stage
     flags |= msa.get_error(clear=True)
     T = w.tokens
     value = world * T * args.steps / (total_ms / 1e3)
     peak, peak_kind = _peaks()
     mean_work = {k: sum(x[k] for x in works) / len(works) for k in works[0]}
     stages = {}
-    for k in ("score", "topk", "attend"):
+    for k in ("score", "attend"):
         if w.topk_given and k != "attend":
             continue
-        gbs = mean_work[k] / (avg_ms[k] / 1e3) / 1e9 if avg_ms[k] > 0 else None
-        stages[k] = {"ms": avg_ms[k], "algorithmic_bytes": mean_work[k], "GB/s": gbs,
+        # the attend kernel also selects (reads the candidate scores, writes the lists)
+        work_k = mean_work[k] + (mean_work["topk"] if k == "attend" and not w.topk_given else 0)
+        gbs = work_k / (avg_ms[k] / 1e3) / 1e9 if avg_ms[k] > 0 else None
+        stages[k] = {"ms": avg_ms[k], "algorithmic_bytes": work_k, "GB/s": gbs,
                      "frac_of_hbm": (gbs / peak) if gbs else None}
+    if not w.topk_given:
+        stages["attend"]["includes"] = "block selection (msa_sparse_decode_select)"
     dominant = max(stages, key=lambda k: stages[k]["ms"])
     d = stages[dominant]
     roofline = {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": d["GB/s"],
@@ -487,11 +523,15 @@ def run_ours(args, rank, world, local):
                 "note": f"of {peak_kind}; achieved = algorithmic bytes per launch / mean "
                         "launch duration (CUDA events around a graph of that kernel's launches "
                         "of the timed steps, replayed after the timed region)"}
-    att = stages["attend"]
-    gathered = {"GB/s": mean_work["attend_kv_bytes"] / (avg_ms["attend"] / 1e3) / 1e9,
+    gathered = {"GB/s": mean_work["attend_kv_bytes"] / (attend_alone_ms / 1e3) / 1e9,
+                "kernel": "attend_kernel on the step's lists (msa_sparse_decode)",
+                "ms": attend_alone_ms,
                 "union_pages_per_step": mean_work["union_pages"],
                 "token_pages_per_step": mean_work["token_pages"]}
     gathered["frac_of_hbm"] = gathered["GB/s"] / peak
+    if not w.topk_given:
+        gathered["fused_select_attend_frac_of_hbm"] = (
+            mean_work["attend_kv_bytes"] / (avg_ms["attend"] / 1e3) / 1e9 / peak)
 
     line = {"impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,

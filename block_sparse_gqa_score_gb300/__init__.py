@@ -34,7 +34,8 @@ TOPK = 16
 GROUP = 16
 MAX_QLEN = 32
 
-__all__ = ["score", "topk", "sparse_decode", "combine", "decode_step", "workspace_bytes",
+__all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "combine", "decode_step",
+           "workspace_bytes",
            "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
 
 
@@ -158,6 +159,44 @@ def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: f
     return out
 
 
+def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_scale: float,
+                         k_scale: float = 1.0, v_scale: float = 1.0,
+                         topk_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                         num_splits: int = 0, workspace: torch.Tensor | None = None,
+                         stream=None):
+    """Selection and attention in one kernel (msa_sparse_decode_select): the
+    top-16 blocks of every (token, KV head) row are selected from `scores`
+    (any strides, as msa_topk) and attended.  Returns (topk [T, Hkv, 16], out)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    # any strided view, as for topk()
+    if not (isinstance(scores, torch.Tensor) and scores.is_cuda and scores.dtype == torch.float32
+            and scores.device == dev):
+        raise TypeError("scores must be a float32 tensor on q's device")
+    if scores.dim() != 3 or scores.shape[0] != Hkv or scores.shape[1] != B * qlen \
+            or scores.shape[2] < S:
+        raise ValueError("scores must be [Hkv, T, >= S]")
+    if topk_out is None:
+        topk_out = torch.empty((B * qlen, Hkv, TOPK), dtype=torch.int32, device=dev)
+    _need(topk_out, "topk_out", (torch.int32,), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,), dev)
+    splits = num_splits if num_splits > 0 else choose_splits(B, qlen, Hkv)
+    need = workspace_bytes(B, qlen, Hq, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    sh, st, sn = scores.stride()
+    status = _lib().msa_sparse_decode_select(
+        q.data_ptr(), kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+        scores.data_ptr(), sh, st, sn, topk_out.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B,
+        qlen, Hq, Hkv, S, NB, float(sm_scale), float(k_scale), float(v_scale), splits,
+        _stream(dev, stream))
+    _native.check(status, "msa_sparse_decode_select")
+    return topk_out, out
+
+
 def combine(workspace: torch.Tensor, tokens: int, num_q_heads: int, num_splits: int,
             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Merge split-K partials (layout of msa_workspace_bytes) into bf16 [T, Hq, 128]."""
@@ -199,17 +238,17 @@ class DecodeBuffers:
 
 def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
                 v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None):
-    """score -> topk -> sparse_decode (-> combine) on one stream, no host sync.
-    Returns (scores, topk, out)."""
+    """score, then selection + attention (msa_sparse_decode_select; -> combine
+    when split) on one stream, no host sync.  Returns (scores, topk, out)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if buffers is None:
         buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
     score(q, kv, block_table, seq_lens, qlen, sm_scale, k_scale, scores=buffers.scores,
           stream=stream)
-    topk(buffers.scores, seq_lens, qlen, out=buffers.topk, stream=stream)
-    sparse_decode(q, kv, block_table, seq_lens, buffers.topk, qlen, sm_scale, k_scale, v_scale,
-                  out=buffers.out, num_splits=buffers.num_splits, workspace=buffers.workspace,
-                  stream=stream)
+    sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale, k_scale,
+                         v_scale, topk_out=buffers.topk, out=buffers.out,
+                         num_splits=buffers.num_splits, workspace=buffers.workspace,
+                         stream=stream)
     return buffers.scores, buffers.topk, buffers.out
 
 

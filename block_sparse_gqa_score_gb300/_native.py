@@ -20,7 +20,7 @@ ERR_TIMEOUT = 0x20
 #: Every symbol include/msa.h declares.
 EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode", "msa_combine", "msa_get_error", "msa_strerror", "msa_version",
-           "msa_sparse_decode_static")
+           "msa_sparse_decode_static", "msa_sparse_decode_select")
 
 _lib = None
 _lock = threading.Lock()
@@ -58,13 +58,16 @@ def load(path: str | None = None):
         lib.msa_sparse_decode.argtypes = [P, P, P, P, P, P, sz, P, i32, i32, i32, i32, i32, i64,
                                           f32, f32, f32, i32, P]
         lib.msa_combine.argtypes = [P, P, i32, i32, i32, P]
+        lib.msa_sparse_decode_select.argtypes = [P, P, P, P, P, i64, i64, i64, P, P, sz, P, i32,
+                                                 i32, i32, i32, i32, i64, f32, f32, f32, i32, P]
         lib.msa_sparse_decode_static.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i64,
                                                  f32, f32, f32, i32, P]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
         for name in ("msa_score", "msa_topk", "msa_choose_splits", "msa_sparse_decode",
-                     "msa_combine", "msa_get_error", "msa_version", "msa_sparse_decode_static"):
+                     "msa_combine", "msa_get_error", "msa_version", "msa_sparse_decode_static",
+                     "msa_sparse_decode_select"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

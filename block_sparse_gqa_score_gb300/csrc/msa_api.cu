@@ -205,16 +205,26 @@ int msa_combine(const void* workspace, void* out, int T, int Hq, int num_splits,
                                        num_splits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int msa_sparse_decode(const void* q, const void* kv, const int32_t* block_table,
-                      const int32_t* seq_lens, const int32_t* topk, void* workspace,
-                      size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
-                      int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
-                      int num_splits, msa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// msa_sparse_decode and msa_sparse_decode_select: `scores` null means `topk`
+// is the input list; otherwise the lists are selected from the strided scores
+// inside the attend kernel and written to `topk`.
+int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
+                  const int32_t* seq_lens, const float* scores, int64_t stride_h,
+                  int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
+                  size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                  int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                  int num_splits, msa_stream_t stream) {
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
   if (!topk || !out || !aligned(topk, 4) || !aligned(out, 16) || !finite_pos(sm_scale) ||
       !finite_pos(k_scale) || !std::isfinite(v_scale) || num_splits < 0 ||
       num_splits > kMaxSplits)
+    return MSA_EINVAL;
+  if (scores && (!aligned(scores, 4) || stride_h < 0 || stride_t < 0 || stride_n < 0))
     return MSA_EINVAL;
   if (B == 0) return MSA_OK;
   DeviceState* dev;
@@ -231,6 +241,11 @@ int msa_sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.topk = topk;
+  p.scores = scores;
+  p.s_stride_h = stride_h;
+  p.s_stride_t = stride_t;
+  p.s_stride_n = stride_n;
+  p.topk_out = scores ? topk : nullptr;
   p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.part_ml = splits > 1 ? static_cast<float*>(workspace) + splits * rows * MSA_HEAD_DIM : nullptr;
   p.out = static_cast<uint16_t*>(out);
@@ -250,6 +265,32 @@ int msa_sparse_decode(const void* q, const void* kv, const int32_t* block_table,
     return from_cuda(
         msa::launch_combine(p.part_o, p.part_ml, static_cast<uint16_t*>(out), rows, splits, s));
   return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int msa_sparse_decode(const void* q, const void* kv, const int32_t* block_table,
+                      const int32_t* seq_lens, const int32_t* topk, void* workspace,
+                      size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                      int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                      int num_splits, msa_stream_t stream) {
+  return sparse_decode(q, kv, block_table, seq_lens, nullptr, 0, 0, 0, const_cast<int32_t*>(topk),
+                       workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream);
+}
+
+int msa_sparse_decode_select(const void* q, const void* kv, const int32_t* block_table,
+                             const int32_t* seq_lens, const float* scores, int64_t stride_h,
+                             int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
+                             size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv,
+                             int S, int64_t num_blocks, float sm_scale, float k_scale,
+                             float v_scale, int num_splits, msa_stream_t stream) {
+  if (!scores) return MSA_EINVAL;
+  return sparse_decode(q, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
+                       workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream);
 }
 
 int msa_get_error(unsigned int* flags, int clear) {

@@ -34,6 +34,7 @@
 //        O = O * alpha + O_page in registers, so O is never rescaled in place.
 #include "msa_device.cuh"
 #include "msa_launch.h"
+#include "msa_select.cuh"
 #include "msa_tcgen05.cuh"
 
 namespace msa {
@@ -54,6 +55,8 @@ constexpr int kTmemCols = 128;                // S^T x 2 buffers, O^T x 2 buffer
 constexpr uint32_t kColS = 0, kColO = 64;
 constexpr float kPShift = 8.f;                // P = 2^(x - m + kPShift)
 constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it by more than this
+// select-then-attend: the (still empty) stage ring is the selector's scratch
+constexpr int kSelectCap = 16384;             // keys cached (64 KiB), then the slots
 
 struct AttendTail {
   uint64_t full[kStages];   // TMA -> S^T issuer
@@ -81,6 +84,7 @@ constexpr int kOffL = kOffMx + 2 * 4 * kGroup * 4;  // running sums [4 warps][16
 constexpr int kOffTail = kOffL + 4 * kGroup * 4;
 constexpr int kSmemBytes = kOffTail + static_cast<int>((sizeof(AttendTail) + 15) / 16 * 16) + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(4 * kSelectCap + 4 * kTopK <= kStages * kStageBytes, "selector scratch fits the ring");
 static_assert(kOffTail % 16 == 0, "mbarriers need 8-byte alignment");
 
 template <int N>
@@ -111,11 +115,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) {
     // this CTA's page list, barriers, and the first loads
     const int L = p.seq_lens[b];
-    pdl_wait();  // the top-k lists come from the previous kernel
-    int n = lane < kTopK ? p.topk[(static_cast<int64_t>(i) * p.Hkv + g) * kTopK + lane] : -1;
+    pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
     const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
     const int pos = seq_ok ? L - p.Q + j : -1;
+    const int64_t list = (static_cast<int64_t>(i) * p.Hkv + g) * kTopK;
+    int n;
+    if (p.scores) {
+      // select this row's blocks here; the stage ring, not yet loaded, is the
+      // scratch, and the fence orders these writes before the TMA loads into it
+      bool nan = false;
+      n = pos >= 0 ? select::select_row(p.scores + g * p.s_stride_h + i * p.s_stride_t,
+                                        p.s_stride_n, pos, lane, reinterpret_cast<uint32_t*>(smem),
+                                        kSelectCap,
+                                        reinterpret_cast<int*>(smem + 4 * kSelectCap), nan)
+                   : -1;
+      if (lane < kTopK) p.topk_out[list + lane] = n;
+      if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+    } else {
+      n = lane < kTopK ? p.topk[list + lane] : -1;
+    }
     int page = -1;
     bool valid = false;
     if (lane < kTopK && pos >= 0) {

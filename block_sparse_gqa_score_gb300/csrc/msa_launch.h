@@ -36,7 +36,13 @@ struct AttendParams {
   const uint16_t* q;           // bf16 bits [T, Hq, 128]
   const int32_t* block_table;  // [B, S]
   const int32_t* seq_lens;     // [B]
-  const int32_t* topk;         // [T, Hkv, 16]
+  const int32_t* topk;         // [T, Hkv, 16]; unused when `scores` is given
+  // select-then-attend: each row's top-k list is selected inside the kernel
+  // from scores[g * s_stride_h + i * s_stride_t + n * s_stride_n] and written
+  // to topk_out [T, Hkv, 16]; nullptr: `topk` is the input list
+  const float* scores;
+  int64_t s_stride_h, s_stride_t, s_stride_n;
+  int32_t* topk_out;
   float* part_o;               // [splits, T, Hq, 128]     (splits > 1)
   float* part_ml;              // [splits, T, Hq, 2]       (splits > 1)
   uint16_t* out;               // bf16 bits [T, Hq, 128]   (splits == 1)

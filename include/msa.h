@@ -10,6 +10,7 @@
  *   msa_topk           top-16 block selection                  (stage 2)
  *   msa_sparse_decode  split-K attention over the selected pages (stage 3)
  *   msa_combine        merge of the split-K partials            (stage 4)
+ *   msa_sparse_decode_select  stages 2 and 3 in one kernel
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -160,9 +161,11 @@ int msa_choose_splits(int B, int Q, int Hkv, int sm_count);
  * (msa_choose_splits); with an effective split count above 1 the partials go
  * to `workspace` and msa_combine is enqueued on `stream` by this call, so
  * `out` is complete when the stream reaches that point either way.
- * Numerics: fp8 K/V widened exactly to fp16, q rows power-of-two scaled to
- * fp16, probabilities rounded to fp16, fp32 accumulation and softmax, output
- * rounded to bf16 (nearest even).
+ * Numerics: the fp8 K and V tiles are tensor-core operands as stored; the
+ * query, scaled per (token, KV head) by a power of two, is the exact sum of
+ * two fp8 e4m3 parts; probabilities P <= 2^8.5 are the sum of two e4m3 parts
+ * (about 8 significant bits); fp32 accumulation and softmax, output rounded
+ * to bf16 (nearest even).
  * Errors: as msa_score, plus null/misaligned topk or out, v_scale not finite,
  * num_splits < 0 or > 16 (MSA_EINVAL), workspace_bytes too small (MSA_ENOSPC).
  * Device: MSA_ERR_TOPK_RANGE / MSA_ERR_TOPK_DUP / MSA_ERR_PAGE_RANGE (entry
@@ -173,6 +176,24 @@ int msa_sparse_decode(const void *q, const void *kv, const int32_t *block_table,
                       size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv,
                       int S, int64_t num_blocks, float sm_scale, float k_scale,
                       float v_scale, int num_splits, msa_stream_t stream);
+
+/*
+ * msa_sparse_decode_select -- stages 2 and 3 in one kernel: each (token, KV
+ * head) row's blocks are selected exactly as msa_topk selects them, from
+ * `scores` read through the element strides (stride_h, stride_t, stride_n),
+ * written to `topk` [T, Hkv, 16], and attended as msa_sparse_decode attends a
+ * given list (the split merge enqueued on `stream` when split).  Saves the
+ * separate selector launch and the re-read of its output; the selection runs
+ * in the attend kernel's prologue, overlapping the previous kernel's tail.
+ * Arguments and errors: as msa_topk for the scores and as msa_sparse_decode
+ * otherwise (`topk` is an output here).
+ */
+int msa_sparse_decode_select(const void *q, const void *kv, const int32_t *block_table,
+                             const int32_t *seq_lens, const float *scores, int64_t stride_h,
+                             int64_t stride_t, int64_t stride_n, int32_t *topk, void *workspace,
+                             size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv,
+                             int S, int64_t num_blocks, float sm_scale, float k_scale,
+                             float v_scale, int num_splits, msa_stream_t stream);
 
 /*
  * msa_combine -- stage 4, merge of split-K partials ("fp32 split-K partials"

@@ -116,6 +116,16 @@ def test_sparse_decode_rejects(lib, kw):
     assert _decode(lib, **kw) == EINVAL
 
 
+def test_select_attend_rejects_missing_scores(lib):
+    f = lib.msa_sparse_decode_select
+    assert f(A, A, A, A, None, 0, 0, 1, A, None, 0, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0, 1.0, 1,
+             None) == EINVAL
+    assert f(A, A, A, A, ctypes.c_void_p((1 << 20) + 2), 0, 0, 1, A, None, 0, A, 16, 4, 64, 4, 8,
+             100, 0.088, 1.0, 1.0, 1, None) == EINVAL      # misaligned scores
+    assert f(A, A, A, A, A, 0, 0, -1, A, None, 0, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0, 1.0, 1,
+             None) == EINVAL                               # negative stride
+
+
 def test_topk_rejects(lib):
     f = lib.msa_topk
     assert f(A, 0, 0, 1, A, A, 16, 4, 4, 8, 8, None) == EINVAL       # k != 16

@@ -202,3 +202,44 @@ def test_bad_indices_are_flagged_and_skipped():
     long[0] = inp.stride * 128 + 1
     msa.topk(torch.zeros((1, 2, inp.stride), device=DEV), long, 1)
     assert msa.get_error() & msa._native.ERR_SEQ_RANGE
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", SMALL_CASES)
+def test_select_attend_matches_the_separate_stages(seq_lens, Q, Hq, Hkv):
+    """msa_sparse_decode_select selects inside the attend kernel: the lists are
+    bit-exact against the oracle given the GPU's scores, and the output has the
+    same bits as msa_sparse_decode on those lists."""
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=107, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax", min_stride=3)
+    scores = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale)
+    splits = 3 if Q == 8 else 0
+    tk, out = msa.sparse_decode_select(inp.q, inp.kv, inp.block_table, inp.seq_lens, scores, Q,
+                                       inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=splits)
+    want = oracle.topk(_np(scores).astype(np.float64), np.array(seq_lens, dtype=np.int32), Q)
+    assert np.array_equal(_np(tk), want)
+    sep = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, tk, Q, inp.sm_scale,
+                            inp.k_scale, inp.v_scale, num_splits=splits)
+    assert torch.equal(out, sep)
+    assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("S,cur_lo", [(40, 17), (300, 200), (700, 600)])
+def test_select_attend_ties_and_strides(S, cur_lo):
+    """Tie-heavy integer scores read through a transposed view; S = 700 takes
+    the selector's path for rows longer than 512 candidates."""
+    g = torch.Generator().manual_seed(S + 1)
+    B, Q, Hq, Hkv = 3, 4, 32, 2
+    seq_lens = torch.randint(cur_lo * 128, S * 128 - 4, (B,), generator=g).tolist()
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=108, device=DEV, min_stride=S)
+    assert inp.stride == S
+    phys = torch.randint(-4, 5, (Hkv, S, B * Q), generator=g).float()
+    phys[0, 5, :] = -0.0
+    phys[1, 7, :] = 0.0
+    scores = phys.to(DEV).transpose(1, 2)           # [Hkv, T, S] view
+    tk, out = msa.sparse_decode_select(inp.q, inp.kv, inp.block_table, inp.seq_lens, scores, Q,
+                                       inp.sm_scale)
+    want = oracle.topk(phys.double().numpy().transpose(0, 2, 1), np.array(seq_lens, dtype=np.int32), Q)
+    assert np.array_equal(_np(tk), want)
+    sep = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, tk, Q, inp.sm_scale)
+    assert torch.equal(out, sep)
+    assert msa.get_error() == 0
