@@ -55,8 +55,9 @@ constexpr int kTmemCols = 128;                // S^T x 2 buffers, O^T x 2 buffer
 constexpr uint32_t kColS = 0, kColO = 64;
 constexpr float kPShift = 8.f;                // P = 2^(x - m + kPShift)
 constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it by more than this
-// select-then-attend: the (still empty) stage ring is the selector's scratch
-constexpr int kSelectCap = 16384;             // keys cached (64 KiB), then the slots
+// select-then-attend: stages 1-2 (stage 0 may already be loading) are the
+// selector's scratch
+constexpr int kSelectCap = 16000;             // keys cached (62.5 KiB), then the slots
 
 struct AttendTail {
   uint64_t full[kStages];   // TMA -> S^T issuer
@@ -84,7 +85,8 @@ constexpr int kOffL = kOffMx + 2 * 4 * kGroup * 4;  // running sums [4 warps][16
 constexpr int kOffTail = kOffL + 4 * kGroup * 4;
 constexpr int kSmemBytes = kOffTail + static_cast<int>((sizeof(AttendTail) + 15) / 16 * 16) + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1024-byte alignment");
-static_assert(4 * kSelectCap + 4 * kTopK <= kStages * kStageBytes, "selector scratch fits the ring");
+static_assert(4 * kSelectCap + 4 * kTopK <= (kStages - 1) * kStageBytes,
+              "selector scratch fits stages 1-2");
 static_assert(kOffTail % 16 == 0, "mbarriers need 8-byte alignment");
 
 template <int N>
@@ -115,20 +117,54 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) {
     // this CTA's page list, barriers, and the first loads
     const int L = p.seq_lens[b];
-    pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
     const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
     const int pos = seq_ok ? L - p.Q + j : -1;
     const int64_t list = (static_cast<int64_t>(i) * p.Hkv + g) * kTopK;
+    // Select mode keeps the current block in every list (first in this CTA's
+    // page order, so it belongs to split 0): its page depends on inputs only,
+    // so it is loaded into stage 0 before waiting for the scores.
+    const int cur = pos >= 0 ? pos / kPage : -1;
+    int cur_page = -1;
+    if (p.scores && cur >= 0 && split == 0) {
+      const int pg = p.block_table[static_cast<int64_t>(b) * p.S + cur];
+      if (pg >= 0 && static_cast<int64_t>(pg) < p.num_blocks) cur_page = pg;
+    }
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&tail->full[s], 1);
+        mbar_init(&tail->empty[s], 1);
+      }
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&tail->s_full[s], 1);
+        mbar_init(&tail->s_empty[s], 4);
+        mbar_init(&tail->p_full[s], 4);
+        mbar_init(&tail->o_full[s], 1);
+        mbar_init(&tail->o_empty[s], 4);
+        mbar_init(&tail->mx_full[s], 4);
+      }
+      mbar_init(&tail->l_full, 4);
+      mbar_init(&tail->finish, kWarps);
+      fence_barrier_init();
+      prefetch_tensormap(&kv_map);
+      if (cur_page >= 0) {
+        const int row = (cur_page * p.Hkv + g) * kPage;
+        mbar_arrive_expect_tx(&tail->full[0], kStageBytes);
+        tma_load_2d(smem, &kv_map, 0, row, &tail->full[0]);
+        tma_load_2d(smem + kHalfTile, &kv_map, kHeadDim, row, &tail->full[0]);
+      }
+    }
+    pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
     int n;
     if (p.scores) {
-      // select this row's blocks here; the stage ring, not yet loaded, is the
-      // scratch, and the fence orders these writes before the TMA loads into it
+      // select this row's blocks here; stages 1-2, not yet loaded, are the
+      // scratch, and the fence orders these writes before the TMA loads into them
       bool nan = false;
+      uint8_t* scratch = smem + kStageBytes;
       n = pos >= 0 ? select::select_row(p.scores + g * p.s_stride_h + i * p.s_stride_t,
-                                        p.s_stride_n, pos, lane, reinterpret_cast<uint32_t*>(smem),
-                                        kSelectCap,
-                                        reinterpret_cast<int*>(smem + 4 * kSelectCap), nan)
+                                        p.s_stride_n, pos, lane,
+                                        reinterpret_cast<uint32_t*>(scratch), kSelectCap,
+                                        reinterpret_cast<int*>(scratch + 4 * kSelectCap), nan)
                    : -1;
       if (lane < kTopK) p.topk_out[list + lane] = n;
       if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);
@@ -160,12 +196,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         valid = false;
       }
     }
+    // page order: the current block first when listed (in select mode it
+    // always is, and may already be loading), then the others ascending; both
+    // modes use this order, so they give the same bits for the same lists
     const unsigned vm = __ballot_sync(0xffffffffu, valid);
-    const int idx = __popc(vm & ((1u << lane) - 1u));
+    const bool front = valid && n == cur;
+    const unsigned fm = __ballot_sync(0xffffffffu, front);
+    const int idx = front ? 0 : __popc(vm & ((1u << lane) - 1u)) + (fm ? 1 : 0);
     const bool mine = valid && (idx % p.splits == split);
     const unsigned mm = __ballot_sync(0xffffffffu, mine);
+    const bool mine_front = (mm & fm) != 0u;
     if (mine) {
-      const int k = __popc(mm & ((1u << lane) - 1u));
+      const int k = front ? 0 : __popc(mm & ~fm & ((1u << lane) - 1u)) + (mine_front ? 1 : 0);
       tail->pages[k] = page;
       tail->blocks[k] = n;
     }
@@ -174,23 +216,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int np = __popc(mm);
       tail->n_pages = np;
       tail->pos = pos;
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(&tail->full[s], 1);
-        mbar_init(&tail->empty[s], 1);
-      }
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(&tail->s_full[s], 1);
-        mbar_init(&tail->s_empty[s], 4);
-        mbar_init(&tail->p_full[s], 4);
-        mbar_init(&tail->o_full[s], 1);
-        mbar_init(&tail->o_empty[s], 4);
-        mbar_init(&tail->mx_full[s], 4);
-      }
-      mbar_init(&tail->l_full, 4);
-      mbar_init(&tail->finish, kWarps);
-      fence_barrier_init();
-      prefetch_tensormap(&kv_map);
-      for (int t = 0; t < np && t < kStages; ++t) {
+      // stage 0 already holds the current block's page when it was loaded early
+      // (it then is page 0 of this list: valid, and split 0 owns it)
+      const int t0 = (cur_page >= 0) ? 1 : 0;
+      for (int t = t0; t < np && t < kStages; ++t) {
         uint8_t* st = smem + t * kStageBytes;
         const int row = (tail->pages[t] * p.Hkv + g) * kPage;
         mbar_arrive_expect_tx(&tail->full[t], kStageBytes);
