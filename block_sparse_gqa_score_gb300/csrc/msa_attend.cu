@@ -121,12 +121,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
     const int pos = seq_ok ? L - p.Q + j : -1;
     const int64_t list = (static_cast<int64_t>(i) * p.Hkv + g) * kTopK;
-    // Select mode keeps the current block in every list (first in this CTA's
-    // page order, so it belongs to split 0): its page depends on inputs only,
-    // so it is loaded into stage 0 before waiting for the scores.
+    // The current block comes first in a CTA's page order when it is listed
+    // (split 0 then owns it), and it always is in select mode and in the
+    // selector's lists.  Its page depends on inputs only, so it is loaded into
+    // stage 0 before waiting for the previous kernel; a given list without it
+    // costs one discarded load.
     const int cur = pos >= 0 ? pos / kPage : -1;
     int cur_page = -1;
-    if (p.scores && cur >= 0 && split == 0) {
+    if (cur >= 0 && split == 0) {
       const int pg = p.block_table[static_cast<int64_t>(b) * p.S + cur];
       if (pg >= 0 && static_cast<int64_t>(pg) < p.num_blocks) cur_page = pg;
     }
@@ -216,9 +218,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int np = __popc(mm);
       tail->n_pages = np;
       tail->pos = pos;
-      // stage 0 already holds the current block's page when it was loaded early
-      // (it then is page 0 of this list: valid, and split 0 owns it)
-      const int t0 = (cur_page >= 0) ? 1 : 0;
+      // stage 0 already holds (or is loading) the current block's page: it is
+      // page 0 of this list when the list has it; otherwise the load lands
+      // unused and stage 0's barrier starts over
+      if (cur_page >= 0 && !mine_front) {
+        if (!mbar_wait(&tail->full[0], 0)) flag_error(p.err, MSA_ERR_TIMEOUT);
+        mbar_inval(&tail->full[0]);
+        mbar_init(&tail->full[0], 1);
+        fence_barrier_init();
+      }
+      const int t0 = (cur_page >= 0 && mine_front) ? 1 : 0;
       for (int t = t0; t < np && t < kStages; ++t) {
         uint8_t* st = smem + t * kStageBytes;
         const int row = (tail->pages[t] * p.Hkv + g) * kPage;

@@ -69,6 +69,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
                : "memory");
 }
 
+// Invalidate an mbarrier that has no pending arrivals or waiters, so that it
+// can be initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -243,3 +243,29 @@ def test_select_attend_ties_and_strides(S, cur_lo):
     sep = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, tk, Q, inp.sm_scale)
     assert torch.equal(out, sep)
     assert msa.get_error() == 0
+
+
+def test_attend_lists_without_the_current_block():
+    """Lists that leave out the current block: the attend loads that block's
+    page speculatively before it sees the list, and must then discard it (and
+    start stage 0 over); the output must still match the oracle."""
+    seq_lens, Q, Hq, Hkv = [3000, 9000, 17000, 700], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=109, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    topk = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(9))
+    for i in range(len(seq_lens) * Q):
+        b, j = divmod(i, Q)
+        pos = seq_lens[b] - Q + j
+        if pos < 0:
+            continue
+        cur = pos // 128
+        row = topk[i]
+        row[row == cur] = -1                          # drop the current block ...
+        if i % 3 == 0 and cur >= 1:
+            row[0, 0] = cur - 1 if (row[0] != cur - 1).all() else row[0, 0]  # ... some rows vary
+    for splits in (1, 3):
+        out = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk.to(DEV), Q,
+                                inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=splits)
+        ref = oracle.attend(to_problem(inp, oracle), topk.numpy())
+        assert_out_close(_np(out), ref, padding_rows(seq_lens, Q))
+        assert msa.get_error() == 0
