@@ -55,9 +55,12 @@ constexpr int kTmemCols = 128;                // S^T x 2 buffers, O^T x 2 buffer
 constexpr uint32_t kColS = 0, kColO = 64;
 constexpr float kPShift = 8.f;                // P = 2^(x - m + kPShift)
 constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it by more than this
-// select-then-attend: stages 1-2 (stage 0 may already be loading) are the
-// selector's scratch
-constexpr int kSelectCap = 16000;             // keys cached (62.5 KiB), then the slots
+// Prologue scratch in the stage ring, before its first loads (stage 0 may
+// already be loading the current block's page): stage 1 holds the selector's
+// keys and slots (select mode), stage 2 a copy of the request's block-table
+// row up to the current block.
+constexpr int kSelectCap = 8000;              // keys cached (31.25 KiB), then the slots
+constexpr int kTableCap = kStageBytes / 4;    // block-table entries copied
 
 struct AttendTail {
   uint64_t full[kStages];   // TMA -> S^T issuer
@@ -85,8 +88,8 @@ constexpr int kOffL = kOffMx + 2 * 4 * kGroup * 4;  // running sums [4 warps][16
 constexpr int kOffTail = kOffL + 4 * kGroup * 4;
 constexpr int kSmemBytes = kOffTail + static_cast<int>((sizeof(AttendTail) + 15) / 16 * 16) + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1024-byte alignment");
-static_assert(4 * kSelectCap + 4 * kTopK <= (kStages - 1) * kStageBytes,
-              "selector scratch fits stages 1-2");
+static_assert(4 * kSelectCap + 4 * kTopK <= kStageBytes, "selector scratch fits stage 1");
+static_assert(kStages >= 3, "prologue scratch uses stages 1 and 2");
 static_assert(kOffTail % 16 == 0, "mbarriers need 8-byte alignment");
 
 template <int N>
@@ -156,11 +159,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(smem + kHalfTile, &kv_map, kHeadDim, row, &tail->full[0]);
       }
     }
+    // the request's block-table row up to the current block, into stage 2
+    int32_t* table_s = reinterpret_cast<int32_t*>(smem + 2 * kStageBytes);
+    const int ncopy = cur < kTableCap ? cur + 1 : 0;
+    for (int e = lane; e < ncopy; e += 32) table_s[e] = p.block_table[static_cast<int64_t>(b) * p.S + e];
+    __syncwarp();
     pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
     int n;
     if (p.scores) {
-      // select this row's blocks here; stages 1-2, not yet loaded, are the
-      // scratch, and the fence orders these writes before the TMA loads into them
+      // select this row's blocks here; stage 1, not yet loaded, is the scratch
       bool nan = false;
       uint8_t* scratch = smem + kStageBytes;
       n = pos >= 0 ? select::select_row(p.scores + g * p.s_stride_h + i * p.s_stride_t,
@@ -170,8 +177,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                    : -1;
       if (lane < kTopK) p.topk_out[list + lane] = n;
       if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);
-      tc::fence_proxy_async_smem();
-      __syncwarp();
     } else {
       n = lane < kTopK ? p.topk[list + lane] : -1;
     }
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       valid = false;
     }
     if (valid) {
-      page = p.block_table[static_cast<int64_t>(b) * p.S + n];
+      page = n < ncopy ? table_s[n] : p.block_table[static_cast<int64_t>(b) * p.S + n];
       if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks) {
         flag_error(p.err, MSA_ERR_PAGE_RANGE);
         valid = false;
@@ -213,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       tail->pages[k] = page;
       tail->blocks[k] = n;
     }
+    // the scratch writes in stages 1-2 come before the TMA loads into them
+    tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       const int np = __popc(mm);
