@@ -366,17 +366,25 @@ def run_ours(args, rank, world, local):
                                               inp.topk, inp.qlen, inp.sm_scale, inp.k_scale,
                                               inp.v_scale, out=bf.out, num_splits=bf.num_splits,
                                               workspace=bf.workspace)]
-        # the selection runs inside the attend kernel (msa_sparse_decode_select)
-        return [lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
-                                  inp.sm_scale, inp.k_scale, scores=bf.scores),
-                lambda: None,
-                lambda: msa.sparse_decode_select(inp.q, inp.kv, inp.block_table, inp.seq_lens,
-                                                 bf.scores, inp.qlen, inp.sm_scale, inp.k_scale,
-                                                 inp.v_scale, topk_out=bf.topk, out=bf.out,
-                                                 num_splits=bf.num_splits,
-                                                 workspace=bf.workspace)]
+        score_call = lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
+                                       inp.sm_scale, inp.k_scale, scores=bf.scores)
+        if fused:   # the selection runs inside the attend kernel (msa_sparse_decode_select)
+            return [score_call, lambda: None,
+                    lambda: msa.sparse_decode_select(inp.q, inp.kv, inp.block_table,
+                                                     inp.seq_lens, bf.scores, inp.qlen,
+                                                     inp.sm_scale, inp.k_scale, inp.v_scale,
+                                                     topk_out=bf.topk, out=bf.out,
+                                                     num_splits=bf.num_splits,
+                                                     workspace=bf.workspace)]
+        return [score_call,
+                lambda: msa.topk(bf.scores, inp.seq_lens, inp.qlen, out=bf.topk),
+                lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk,
+                                          inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
+                                          out=bf.out, num_splits=bf.num_splits,
+                                          workspace=bf.workspace)]
 
-    launches_per_step = (1 if w.topk_given else 2) + (1 if splits > 1 else 0)
+    fused = (not w.topk_given) and msa.fused_selection(first.stride)
+    launches_per_step = (1 if w.topk_given else (2 if fused else 3)) + (1 if splits > 1 else 0)
 
     # warm-up (eager), then the per-layer work figures from the real top-k lists
     msa.get_error(clear=True)
@@ -450,8 +458,8 @@ def run_ours(args, rank, world, local):
     avg_ms = {k: 0.0 for k in stage_names}
     reps_stage = min(args.steps, chunk)
     for s_i, k in enumerate(stage_names):
-        if k == "topk" or (w.topk_given and k != "attend"):
-            continue   # the selection is part of the attend kernel
+        if (k == "topk" and fused) or (w.topk_given and k != "attend"):
+            continue   # fused: the selection is part of the attend kernel
         try:
             g = capture(reps_stage, which=(s_i,)) if graphs else None
         except Exception:  # pragma: no cover
@@ -473,7 +481,7 @@ def run_ours(args, rank, world, local):
     # the attend on its own (msa_sparse_decode over the lists the step selected),
     # the kernel the gathered-KV figure is defined on
     attend_alone_ms = avg_ms["attend"]
-    if not w.topk_given:
+    if fused:
         def plain(l):
             inp, bf = layers[l], bufs[l]
             msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk, inp.qlen,
@@ -505,15 +513,15 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = _peaks()
     mean_work = {k: sum(x[k] for x in works) / len(works) for k in works[0]}
     stages = {}
-    for k in ("score", "attend"):
-        if w.topk_given and k != "attend":
+    for k in ("score", "topk", "attend"):
+        if (w.topk_given and k != "attend") or (k == "topk" and fused):
             continue
-        # the attend kernel also selects (reads the candidate scores, writes the lists)
-        work_k = mean_work[k] + (mean_work["topk"] if k == "attend" and not w.topk_given else 0)
+        # fused: the attend kernel also selects (reads the candidates, writes the lists)
+        work_k = mean_work[k] + (mean_work["topk"] if k == "attend" and fused else 0)
         gbs = work_k / (avg_ms[k] / 1e3) / 1e9 if avg_ms[k] > 0 else None
         stages[k] = {"ms": avg_ms[k], "algorithmic_bytes": work_k, "GB/s": gbs,
                      "frac_of_hbm": (gbs / peak) if gbs else None}
-    if not w.topk_given:
+    if fused:
         stages["attend"]["includes"] = "block selection (msa_sparse_decode_select)"
     dominant = max(stages, key=lambda k: stages[k]["ms"])
     d = stages[dominant]
@@ -529,7 +537,7 @@ def run_ours(args, rank, world, local):
                 "union_pages_per_step": mean_work["union_pages"],
                 "token_pages_per_step": mean_work["token_pages"]}
     gathered["frac_of_hbm"] = gathered["GB/s"] / peak
-    if not w.topk_given:
+    if fused:
         gathered["fused_select_attend_frac_of_hbm"] = (
             mean_work["attend_kv_bytes"] / (avg_ms["attend"] / 1e3) / 1e9 / peak)
 

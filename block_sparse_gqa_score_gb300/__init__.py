@@ -35,7 +35,7 @@ GROUP = 16
 MAX_QLEN = 32
 
 __all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "combine", "decode_step",
-           "workspace_bytes",
+           "fused_selection", "FUSED_MAX_BLOCKS", "workspace_bytes",
            "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
 
 
@@ -159,6 +159,18 @@ def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: f
     return out
 
 
+#: Rows of at most this many candidate blocks are selected inside the attend
+#: kernel (the selector keeps them in registers there); longer rows go through
+#: the selector kernel, which holds up to 2048 candidates in registers.
+FUSED_MAX_BLOCKS = 512
+
+
+def fused_selection(stride: int) -> bool:
+    """Whether decode_step selects inside the attend kernel for a block table of
+    `stride` columns (the longest possible row)."""
+    return stride <= FUSED_MAX_BLOCKS
+
+
 def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_scale: float,
                          k_scale: float = 1.0, v_scale: float = 1.0,
                          topk_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
@@ -238,17 +250,25 @@ class DecodeBuffers:
 
 def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
                 v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None):
-    """score, then selection + attention (msa_sparse_decode_select; -> combine
-    when split) on one stream, no host sync.  Returns (scores, topk, out)."""
+    """score, then selection + attention on one stream, no host sync: in one
+    kernel (msa_sparse_decode_select) while rows have at most FUSED_MAX_BLOCKS
+    candidate blocks, else msa_topk then msa_sparse_decode (-> combine when
+    split).  Returns (scores, topk, out)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if buffers is None:
         buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
     score(q, kv, block_table, seq_lens, qlen, sm_scale, k_scale, scores=buffers.scores,
           stream=stream)
-    sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale, k_scale,
-                         v_scale, topk_out=buffers.topk, out=buffers.out,
-                         num_splits=buffers.num_splits, workspace=buffers.workspace,
-                         stream=stream)
+    if fused_selection(S):
+        sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale,
+                             k_scale, v_scale, topk_out=buffers.topk, out=buffers.out,
+                             num_splits=buffers.num_splits, workspace=buffers.workspace,
+                             stream=stream)
+    else:
+        topk(buffers.scores, seq_lens, qlen, out=buffers.topk, stream=stream)
+        sparse_decode(q, kv, block_table, seq_lens, buffers.topk, qlen, sm_scale, k_scale,
+                      v_scale, out=buffers.out, num_splits=buffers.num_splits,
+                      workspace=buffers.workspace, stream=stream)
     return buffers.scores, buffers.topk, buffers.out
 
 

@@ -132,7 +132,8 @@ int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
   const int64_t units = static_cast<int64_t>(B) * Q * Hkv;  // one CTA per (token, KV head)
   const int64_t slots = 2 * static_cast<int64_t>(sm_count);  // two CTAs per SM
   if (units * 4 >= slots * 3) return 1;
-  int64_t s = (slots + units - 1) / units;
+  // as many splits as still fit one wave of resident CTAs
+  int64_t s = slots / units;
   if (s > 8) s = 8;
   return static_cast<int>(s < 1 ? 1 : s);
 }

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // select this row's blocks here; stage 1, not yet loaded, is the scratch
       bool nan = false;
       uint8_t* scratch = smem + kStageBytes;
-      n = pos >= 0 ? select::select_row(p.scores + g * p.s_stride_h + i * p.s_stride_t,
+      n = pos >= 0 ? select::select_row<16>(p.scores + g * p.s_stride_h + i * p.s_stride_t,
                                         p.s_stride_n, pos, lane,
                                         reinterpret_cast<uint32_t*>(scratch), kSelectCap,
                                         reinterpret_cast<int*>(scratch + 4 * kSelectCap), nan)

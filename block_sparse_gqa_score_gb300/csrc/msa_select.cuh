@@ -18,8 +18,9 @@
 // >= tau: they are then the kept set, with no tie at its boundary.  Without an
 // early stop tau ends as the 15th-largest key.  Keys > tau are all kept and the
 // lowest-index keys == tau fill the rest, in one ordered sweep.  Rows of up to
-// 512 candidates live in registers (8 or 16 per lane), longer rows in the
-// caller's shared scratch when they fit, else they are re-read.
+// 2048 candidates live in registers (8 to 64 per lane) during the search,
+// longer rows in the caller's shared scratch when they fit, else they are
+// re-read.
 #pragma once
 
 #include "msa_device.cuh"
@@ -114,9 +115,12 @@ __device__ __forceinline__ uint32_t tau_in_memory(KeyAt& key_at, int cur, int la
 
 // The kept blocks of a row whose token sits at causal position pos >= 0:
 // returns the k-th kept block (ascending, cur last, -1 padded) in lane k < 16,
-// -1 in lanes 16-31.  srow[n * stride_n] is the score of block n.  `keys` is
+// -1 in lanes 16-31.  kMaxRegKeys (16, 32 or 64) bounds the keys a lane holds
+// in registers, i.e. the register pressure the caller can afford.
+// srow[n * stride_n] is the score of block n.  `keys` is
 // shared scratch for `cap` >= 512 keys, `slots` shared scratch for 16 ints
 // (both used only by this warp).  `nan` is set when a score is NaN.
+template <int kMaxRegKeys>
 __device__ __forceinline__ int select_row(const float* __restrict__ srow, int64_t stride_n, int pos,
                                           int lane, uint32_t* keys, int cap, int* slots,
                                           bool& nan) {
@@ -129,6 +133,10 @@ __device__ __forceinline__ int select_row(const float* __restrict__ srow, int64_
     tau = tau_in_registers<8>(load_key, keys, cur, lane);
   } else if (cur <= 32 * 16) {
     tau = tau_in_registers<16>(load_key, keys, cur, lane);
+  } else if (kMaxRegKeys >= 32 && cur <= 32 * 32 && cap >= 32 * 32) {
+    tau = tau_in_registers<(kMaxRegKeys >= 32 ? 32 : 16)>(load_key, keys, cur, lane);
+  } else if (kMaxRegKeys >= 64 && cur <= 32 * 64 && cap >= 32 * 64) {
+    tau = tau_in_registers<(kMaxRegKeys >= 64 ? 64 : 16)>(load_key, keys, cur, lane);
   } else {
     if (cached)
       for (int n = lane; n < cur; n += 32) keys[n] = load_key(n);

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
   }
   const float* srow = p.scores + g * p.stride_h + static_cast<int64_t>(i) * p.stride_t;
   bool nan = false;
-  const int v = select::select_row(srow, p.stride_n, pos, lane, s_keys[warp], kCache,
+  const int v = select::select_row<64>(srow, p.stride_n, pos, lane, s_keys[warp], kCache,
                                    s_slots[warp], nan);
   if (lane < kTopK) out[lane] = v;
   if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);

@@ -185,6 +185,9 @@ int msa_sparse_decode(const void *q, const void *kv, const int32_t *block_table,
  * given list (the split merge enqueued on `stream` when split).  Saves the
  * separate selector launch and the re-read of its output; the selection runs
  * in the attend kernel's prologue, overlapping the previous kernel's tail.
+ * Rows of more than 512 candidate blocks are selected from shared memory
+ * there, which is slower than msa_topk's register paths (up to 2048): for long
+ * contexts msa_topk followed by msa_sparse_decode is the faster pair.
  * Arguments and errors: as msa_topk for the scores and as msa_sparse_decode
  * otherwise (`topk` is an output here).
  */
