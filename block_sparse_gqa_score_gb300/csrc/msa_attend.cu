@@ -58,9 +58,9 @@ constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it 
 // Prologue scratch in the stage ring, before its first loads (stage 0 may
 // already be loading the current block's page): stage 1 holds the selector's
 // keys and slots (select mode), stage 2 a copy of the request's block-table
-// row up to the current block.
+// row (its first kTableCopy entries; later blocks are read from global memory).
 constexpr int kSelectCap = 8000;              // keys cached (31.25 KiB), then the slots
-constexpr int kTableCap = kStageBytes / 4;    // block-table entries copied
+constexpr int kTableCopy = 512;               // 16 loads per lane, all in flight together
 
 struct AttendTail {
   uint64_t full[kStages];   // TMA -> S^T issuer
@@ -90,6 +90,7 @@ constexpr int kSmemBytes = kOffTail + static_cast<int>((sizeof(AttendTail) + 15)
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(4 * kSelectCap + 4 * kTopK <= kStageBytes, "selector scratch fits stage 1");
 static_assert(kStages >= 3, "prologue scratch uses stages 1 and 2");
+static_assert(4 * kTableCopy <= kStageBytes && kTableCopy % 32 == 0, "block-table copy fits stage 2");
 static_assert(kOffTail % 16 == 0, "mbarriers need 8-byte alignment");
 
 template <int N>
@@ -118,8 +119,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- prologue ------------------------------------------------------------------
   if (warp == 0) {
-    // this CTA's page list, barriers, and the first loads
+    // this CTA's page list, barriers, and the first loads.  The request's
+    // block-table row goes into stage 2 while seq_lens is read: every lane
+    // has all its loads in flight at once, so the row costs one round trip.
+    int32_t* table_s = reinterpret_cast<int32_t*>(smem + 2 * kStageBytes);
+    const int32_t* trow = p.block_table + static_cast<int64_t>(b) * p.S;
+    const int ncopy = p.S < kTableCopy ? p.S : kTableCopy;
     const int L = p.seq_lens[b];
+    {
+      int32_t v[kTableCopy / 32];
+#pragma unroll
+      for (int k = 0; k < kTableCopy / 32; ++k) v[k] = 32 * k + lane < ncopy ? trow[32 * k + lane] : 0;
+#pragma unroll
+      for (int k = 0; k < kTableCopy / 32; ++k)
+        if (32 * k + lane < ncopy) table_s[32 * k + lane] = v[k];
+    }
+    __syncwarp();
     const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
     const int pos = seq_ok ? L - p.Q + j : -1;
@@ -132,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cur = pos >= 0 ? pos / kPage : -1;
     int cur_page = -1;
     if (cur >= 0 && split == 0) {
-      const int pg = p.block_table[static_cast<int64_t>(b) * p.S + cur];
+      const int pg = cur < ncopy ? table_s[cur] : trow[cur];
       if (pg >= 0 && static_cast<int64_t>(pg) < p.num_blocks) cur_page = pg;
     }
     if (lane == 0) {
@@ -159,11 +174,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(smem + kHalfTile, &kv_map, kHeadDim, row, &tail->full[0]);
       }
     }
-    // the request's block-table row up to the current block, into stage 2
-    int32_t* table_s = reinterpret_cast<int32_t*>(smem + 2 * kStageBytes);
-    const int ncopy = cur < kTableCap ? cur + 1 : 0;
-    for (int e = lane; e < ncopy; e += 32) table_s[e] = p.block_table[static_cast<int64_t>(b) * p.S + e];
-    __syncwarp();
     pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
     int n;
     if (p.scores) {
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       valid = false;
     }
     if (valid) {
-      page = n < ncopy ? table_s[n] : p.block_table[static_cast<int64_t>(b) * p.S + n];
+      page = n < ncopy ? table_s[n] : trow[n];
       if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks) {
         flag_error(p.err, MSA_ERR_PAGE_RANGE);
         valid = false;
