@@ -200,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           valid = true;
       }
     }
-    // a block listed again at a later slot is dropped
-    const unsigned same = __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
+    // a block listed again at a later slot is dropped (a given list only: the
+    // selector's lists hold distinct blocks)
+    const unsigned same = p.scores ? 0u : __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
     if (valid && (same & ((1u << lane) - 1u))) {
       flag_error(p.err, MSA_ERR_TOPK_DUP);
       valid = false;
