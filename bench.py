@@ -44,6 +44,7 @@ import torch  # noqa: E402
 METRIC = "sparse-decode query-tokens/s per layer"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_SUSTAINED_TFLOPS = 1700.0   # sustained dense bf16 GEMM rate of a GB300, when unmeasured
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -100,6 +101,19 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def _fp8_tensor_peak():
+    """Dense fp8 tensor peak in TFLOP/s: the measured sustained bf16 GEMM rate
+    (the kernels are timed in long back-to-back loops) times 2, the nominal
+    fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return 2.0 * float(d["bf16_tflops_sustained"]), "measured (bf16 sustained x 2)"
+    except Exception:
+        return 2.0 * FALLBACK_BF16_SUSTAINED_TFLOPS, "fallback (bf16 sustained x 2)"
 
 
 class ClockSampler:
@@ -226,6 +240,9 @@ def _work(inp, topk_cpu: np.ndarray | None):
                 cur = pos // 128
                 cand += cur if cur + 1 > 16 else 0
     topk = cand * Hkv * 4 + T * Hkv * 16 * 4
+    # the scorer's products: every visible page-head's 128 keys against its
+    # group's 16 heads x Q tokens, 128-dim dot products
+    score_flops = sum(pages) * Hkv * 2.0 * 128 * 128 * 16 * Q
     union = per_token = 0
     if topk_cpu is not None:
         for b in range(B):
@@ -237,7 +254,7 @@ def _work(inp, topk_cpu: np.ndarray | None):
                 per_token += len(ids)
     attend = union * 32768 + 2 * q_bytes + T * Hkv * 16 * 4
     return {"score": score, "topk": topk, "attend": attend, "union_pages": union,
-            "token_pages": per_token, "attend_kv_bytes": union * 32768}
+            "token_pages": per_token, "attend_kv_bytes": union * 32768, "score_flops": score_flops}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -523,14 +540,29 @@ def run_ours(args, rank, world, local):
                      "frac_of_hbm": (gbs / peak) if gbs else None}
     if fused:
         stages["attend"]["includes"] = "block selection (msa_sparse_decode_select)"
+    tpeak, tpeak_kind = _fp8_tensor_peak()
+    if "score" in stages and avg_ms["score"] > 0:
+        tf = mean_work["score_flops"] / (avg_ms["score"] / 1e3) / 1e12
+        stages["score"].update({"algorithmic_tflop": mean_work["score_flops"] / 1e12,
+                                "TFLOP/s": tf, "frac_of_fp8_tensor": tf / tpeak})
     dominant = max(stages, key=lambda k: stages[k]["ms"])
     d = stages[dominant]
-    roofline = {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": d["GB/s"],
-                "peak": peak, "unit": "GB/s", "frac": d["frac_of_hbm"],
-                "traffic": _traffic_from_profiles(dominant, name), "peak_kind": peak_kind,
-                "note": f"of {peak_kind}; achieved = algorithmic bytes per launch / mean "
-                        "launch duration (CUDA events around a graph of that kernel's launches "
-                        "of the timed steps, replayed after the timed region)"}
+    note = ("achieved = algorithmic {} per launch / mean launch duration (CUDA events around a "
+            "graph of that kernel's launches of the timed steps, replayed after the timed region)")
+    # the scorer's intensity is 32 Q flop per K byte: above the fp8 ridge point
+    # (peak flops / peak bytes) its roofline is the tensor peak
+    if (dominant == "score" and mean_work["score_flops"] / mean_work["score"]
+            > tpeak * 1e12 / (peak * 1e9)):
+        roofline = {"bound": "tensor", "kernel": "score_kernel", "achieved": d["TFLOP/s"],
+                    "peak": tpeak, "unit": "TFLOP/s", "frac": d["frac_of_fp8_tensor"],
+                    "traffic": _traffic_from_profiles(dominant, name), "peak_kind": tpeak_kind,
+                    "note": f"of {tpeak_kind}; " + note.format("flops (useful products; the "
+                            "exact bf16 query as two fp8 parts doubles the executed MMA work)")}
+    else:
+        roofline = {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": d["GB/s"],
+                    "peak": peak, "unit": "GB/s", "frac": d["frac_of_hbm"],
+                    "traffic": _traffic_from_profiles(dominant, name), "peak_kind": peak_kind,
+                    "note": f"of {peak_kind}; " + note.format("bytes")}
     gathered = {"GB/s": mean_work["attend_kv_bytes"] / (attend_alone_ms / 1e3) / 1e9,
                 "kernel": "attend_kernel on the step's lists (msa_sparse_decode)",
                 "ms": attend_alone_ms,
