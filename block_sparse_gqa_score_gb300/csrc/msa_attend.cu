@@ -287,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(st + kHalfTile, &kv_map, kHeadDim, row, &tail->full[s]);
         issued = t + 1;
       }
-      // every load of this CTA is issued: the next kernel may start its CTAs
-      pdl_trigger();
       // the loads still in flight land before shared memory can be released
       for (int t = issued - kStages; t < issued; ++t)
         if (t >= 0) (void)mbar_wait(&tail->full[t % kStages], (t / kStages) & 1);
+      // every load of this CTA has landed: the next kernel may start its CTAs
+      pdl_trigger();
       mbar_arrive(&tail->finish);
     }
   } else if (warp == 1) {

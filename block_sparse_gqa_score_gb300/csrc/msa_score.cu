@@ -313,12 +313,11 @@ __global__ void __maxnreg__(128)
                     &tail->full[s]);
         ++vp;
       }
-      // every load of this CTA is issued: the next kernel may start its CTAs
-      // (its prologue then overlaps this kernel's last pages)
-      pdl_trigger();
       // the last loads in flight land before shared memory can be released
       for (int t = vp - G.stages; t < vp; ++t)
         if (t >= 0) (void)mbar_wait(&tail->full[t % G.stages], (t / G.stages) & 1);
+      // every load of this CTA has landed: the next kernel may start its CTAs
+      pdl_trigger();
       mbar_arrive(&tail->finish);
     }
   } else if (warp == 1) {
