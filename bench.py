@@ -226,7 +226,7 @@ def _traffic_from_profiles(stage: str, workload: str):
 # ----------------------------------------------------------------------------- work accounting
 
 def _work(inp, topk_cpu: np.ndarray | None):
-    """Algorithmic bytes per launch of each stage (the figures the design doc defines)."""
+    """Algorithmic bytes per launch of each stage, and the scorer's useful flops."""
     B, Q, Hq, Hkv, S = inp.batch, inp.qlen, inp.num_q_heads, inp.num_kv_heads, inp.stride
     T = B * Q
     pages = [math.ceil(L / 128) for L in inp.seq_lens_list]
