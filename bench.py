@@ -225,7 +225,7 @@ def _traffic_from_profiles(stage: str, workload: str):
 
 # ----------------------------------------------------------------------------- work accounting
 
-def _work(inp, topk_cpu: np.ndarray | None):
+def _work(inp, topk_cpu: np.ndarray | None, reads_lists: bool = True):
     """Algorithmic bytes per launch of each stage, and the scorer's useful flops."""
     B, Q, Hq, Hkv, S = inp.batch, inp.qlen, inp.num_q_heads, inp.num_kv_heads, inp.stride
     T = B * Q
@@ -252,7 +252,7 @@ def _work(inp, topk_cpu: np.ndarray | None):
                 ids = ids[ids >= 0]
                 union += len(np.unique(ids))
                 per_token += len(ids)
-    attend = union * 32768 + 2 * q_bytes + T * Hkv * 16 * 4
+    attend = union * 32768 + 2 * q_bytes + (T * Hkv * 16 * 4 if reads_lists else 0)
     return {"score": score, "topk": topk, "attend": attend, "union_pages": union,
             "token_pages": per_token, "attend_kv_bytes": union * 32768, "score_flops": score_flops}
 
@@ -272,7 +272,7 @@ def run_reference(args, rank, world):
     units = [(b, g) for b in range(inp.batch) for g in range(inp.num_kv_heads)
              if inp.seq_lens_list[b] > 0]
 
-    given = inp.topk.numpy() if w.topk_given else None
+    given = _given_lists(w, inp)
 
     def step(k):
         b, g = units[k % len(units)]
@@ -294,11 +294,25 @@ def run_reference(args, rank, world):
                              "sample": "one (request, KV head) unit per step, round robin: "
                                        + ("attention of its query rows x 16 heads over the "
                                           "given top-k" if w.topk_given else
+                                          "attention of its query rows x 16 heads over every "
+                                          "visible block" if w.dense else
                                           "scores of all its visible blocks, selection of its "
                                           "query rows, attention of its query rows x 16 heads")
                                        + "; counted as qlen/Hkv query tokens"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+def _given_lists(w, inp):
+    """The lists the oracle attends over when it does not select them: the
+    drawn top-k (attend-only workloads) or every visible block (dense decode)."""
+    if w.topk_given:
+        return inp.topk.cpu().numpy()
+    if w.dense:
+        from block_sparse_gqa_score_gb300 import workloads as wl
+        return wl.all_visible_lists(inp.seq_lens_list, inp.qlen, inp.num_kv_heads,
+                                    inp.stride).numpy()
+    return None
 
 
 def _problem(inp, oracle):
@@ -327,7 +341,7 @@ def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
     oracle.attend_rows(p, full, rows, nthreads)
 
 
-def cpu_baseline(inp, w, topk_cpu, budget_s: float = 12.0):
+def cpu_baseline(inp, w, lists, budget_s: float = 12.0):
     """The oracle timed on this host on a bounded sample of the workload."""
     import oracle
     p = _problem(inp, oracle)
@@ -337,14 +351,16 @@ def cpu_baseline(inp, w, topk_cpu, budget_s: float = 12.0):
     done = 0
     t0 = time.perf_counter()
     for b, g in units:
-        _oracle_unit(p, inp, oracle, b, g, cores, topk_cpu if w.topk_given else None)
+        _oracle_unit(p, inp, oracle, b, g, cores, lists)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     tokens = done * inp.qlen / inp.num_kv_heads
+    what = ("attend only, given top-k" if w.topk_given else "dense attend, every visible block"
+            if w.dense else "score, select, attend")
     sample = (f"{done} of {len(units)} (request, KV head) units of layer 0, each the whole "
-              f"oracle pipeline ({'attend only, given top-k' if w.topk_given else 'score, select, attend'})")
+              f"oracle pipeline ({what})")
     return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": sample, "seconds": dt}
 
@@ -371,12 +387,19 @@ def run_ours(args, rank, world, local):
     n_layers = max(2, math.ceil(4 * l2 / max(layer_bytes, 1)))
     layers = [first] + [wl.make_inputs(w, device=dev, layer=l) for l in range(1, n_layers)]
     splits = msa.choose_splits(w.batch, w.qlen, w.num_kv_heads, props.multi_processor_count)
+    if w.dense:   # the split count of dense decode follows the block table's stride
+        splits = max(msa.dense_splits(inp.stride) for inp in layers)
     bufs = [msa.DecodeBuffers.allocate(w.batch, w.qlen, w.num_q_heads, w.num_kv_heads,
                                        inp.stride, dev, splits) for inp in layers]
     stream = torch.cuda.Stream(dev)
 
     def stage_calls(l):
         inp, bf = layers[l], bufs[l]
+        if w.dense:
+            return [lambda: None, lambda: None,
+                    lambda: msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                             inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
+                                             out=bf.out, workspace=bf.workspace)]
         if w.topk_given:
             return [lambda: None, lambda: None,
                     lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
@@ -400,8 +423,9 @@ def run_ours(args, rank, world, local):
                                           out=bf.out, num_splits=bf.num_splits,
                                           workspace=bf.workspace)]
 
-    fused = (not w.topk_given) and msa.fused_selection(first.stride)
-    launches_per_step = (1 if w.topk_given else (2 if fused else 3)) + (1 if splits > 1 else 0)
+    attend_only = w.topk_given or w.dense
+    fused = (not attend_only) and msa.fused_selection(first.stride)
+    launches_per_step = (1 if attend_only else (2 if fused else 3)) + (1 if splits > 1 else 0)
 
     # warm-up (eager), then the per-layer work figures from the real top-k lists
     msa.get_error(clear=True)
@@ -411,8 +435,11 @@ def run_ours(args, rank, world, local):
                 f()
     torch.cuda.synchronize(dev)
     flags = msa.get_error(clear=True)
-    works = [_work(inp, (inp.topk if w.topk_given else bf.topk).cpu().numpy())
-             for inp, bf in zip(layers, bufs)]
+    works = []
+    for inp, bf in zip(layers, bufs):
+        lists = _given_lists(w, inp)
+        works.append(_work(inp, lists if lists is not None else bf.topk.cpu().numpy(),
+                           reads_lists=not w.dense))
 
     # the timed region: CUDA-graph replays of `chunk` steps, kernels only
     chunk = max(1, min(args.steps, args.graph_chunk))
@@ -475,7 +502,7 @@ def run_ours(args, rank, world, local):
     avg_ms = {k: 0.0 for k in stage_names}
     reps_stage = min(args.steps, chunk)
     for s_i, k in enumerate(stage_names):
-        if (k == "topk" and fused) or (w.topk_given and k != "attend"):
+        if (k == "topk" and fused) or (attend_only and k != "attend"):
             continue   # fused: the selection is part of the attend kernel
         try:
             g = capture(reps_stage, which=(s_i,)) if graphs else None
@@ -531,7 +558,7 @@ def run_ours(args, rank, world, local):
     mean_work = {k: sum(x[k] for x in works) / len(works) for k in works[0]}
     stages = {}
     for k in ("score", "topk", "attend"):
-        if (w.topk_given and k != "attend") or (k == "topk" and fused):
+        if (attend_only and k != "attend") or (k == "topk" and fused):
             continue
         # fused: the attend kernel also selects (reads the candidates, writes the lists)
         work_k = mean_work[k] + (mean_work["topk"] if k == "attend" and fused else 0)
@@ -564,7 +591,8 @@ def run_ours(args, rank, world, local):
                     "traffic": _traffic_from_profiles(dominant, name), "peak_kind": peak_kind,
                     "note": f"of {peak_kind}; " + note.format("bytes")}
     gathered = {"GB/s": mean_work["attend_kv_bytes"] / (attend_alone_ms / 1e3) / 1e9,
-                "kernel": "attend_kernel on the step's lists (msa_sparse_decode)",
+                "kernel": ("attend_kernel over every visible block (msa_dense_decode)"
+                           if w.dense else "attend_kernel on the step's lists (msa_sparse_decode)"),
                 "ms": attend_alone_ms,
                 "union_pages_per_step": mean_work["union_pages"],
                 "token_pages_per_step": mean_work["token_pages"]}
@@ -590,8 +618,10 @@ def run_ours(args, rank, world, local):
         line["e2e"] = _e2e(msa, w, layers, bufs, stream, dev, world, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp0 = layers[0]
-        tk = (inp0.topk if w.topk_given else bufs[0].topk).cpu().numpy()
-        line["cpu_baseline"] = cpu_baseline(_to_cpu(inp0), w, tk)
+        lists = _given_lists(w, inp0)
+        if lists is None:   # the step's own selection
+            lists = bufs[0].topk.cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline(_to_cpu(inp0), w, lists)
     if rank == 0:
         print(json.dumps(line))
 
@@ -658,6 +688,10 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
             msa.sparse_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], v["topk"],
                               inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
                               num_splits=bf.num_splits, workspace=bf.workspace)
+        elif w.dense:
+            msa.dense_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
+                             inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
+                             workspace=bf.workspace)
         else:
             msa.decode_step(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
                             inp.sm_scale, inp.k_scale, inp.v_scale, buffers=bf)

@@ -34,7 +34,8 @@ TOPK = 16
 GROUP = 16
 MAX_QLEN = 32
 
-__all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "combine", "decode_step",
+__all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "dense_decode", "dense_splits",
+           "combine", "decode_step",
            "fused_selection", "FUSED_MAX_BLOCKS", "workspace_bytes",
            "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
 
@@ -156,6 +157,37 @@ def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: f
                                   out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
                                   float(k_scale), float(v_scale), splits, _stream(dev, stream))
     _native.check(st, "msa_sparse_decode")
+    return out
+
+
+def dense_splits(stride: int) -> int:
+    """Split count of dense_decode for a block table of `stride` columns (0:
+    longer than dense_decode takes)."""
+    return int(_lib().msa_dense_splits(int(stride)))
+
+
+def dense_decode(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
+                 v_scale: float = 1.0, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Attention over every visible block, bf16 [T, Hq, 128] (msa_dense_decode;
+    with more than one split the merge runs on the same stream)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,), dev)
+    splits = dense_splits(S)
+    if splits == 0:
+        raise ValueError("dense_decode takes block tables of at most 2048 columns")
+    need = workspace_bytes(B, qlen, Hq, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib().msa_dense_decode(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(),
+                                 seq_lens.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B, qlen, Hq,
+                                 Hkv, S, NB, float(sm_scale), float(k_scale), float(v_scale),
+                                 _stream(dev, stream))
+    _native.check(st, "msa_dense_decode")
     return out
 
 

@@ -20,7 +20,8 @@ ERR_TIMEOUT = 0x20
 #: Every symbol include/msa.h declares.
 EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode", "msa_combine", "msa_get_error", "msa_strerror", "msa_version",
-           "msa_sparse_decode_static", "msa_sparse_decode_select")
+           "msa_sparse_decode_static", "msa_sparse_decode_select", "msa_dense_splits",
+           "msa_dense_decode")
 
 _lib = None
 _lock = threading.Lock()
@@ -62,12 +63,15 @@ def load(path: str | None = None):
                                                  i32, i32, i32, i32, i64, f32, f32, f32, i32, P]
         lib.msa_sparse_decode_static.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i64,
                                                  f32, f32, f32, i32, P]
+        lib.msa_dense_splits.argtypes = [i32]
+        lib.msa_dense_decode.argtypes = [P, P, P, P, P, sz, P, i32, i32, i32, i32, i32, i64, f32,
+                                         f32, f32, P]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
         for name in ("msa_score", "msa_topk", "msa_choose_splits", "msa_sparse_decode",
                      "msa_combine", "msa_get_error", "msa_version", "msa_sparse_decode_static",
-                     "msa_sparse_decode_select"):
+                     "msa_sparse_decode_select", "msa_dense_splits", "msa_dense_decode"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -210,18 +210,30 @@ int msa_combine(const void* workspace, void* out, int T, int Hq, int num_splits,
 
 namespace {
 
-// msa_sparse_decode and msa_sparse_decode_select: `scores` null means `topk`
-// is the input list; otherwise the lists are selected from the strided scores
-// inside the attend kernel and written to `topk`.
+// Dense decode's split of a row's S blocks: up to 16 CTAs, each over a range
+// of at most 128 consecutive blocks (a CTA's page list holds 128).
+constexpr int kDenseMaxSpan = 128;
+
+void dense_split(int S, int* nsplit, int* span) {
+  const int groups = (S + MSA_TOPK - 1) / MSA_TOPK;  // 16-block groups
+  *nsplit = groups < 1 ? 1 : (groups > kMaxSplits ? kMaxSplits : groups);
+  *span = (S + *nsplit - 1) / *nsplit;
+}
+
+// msa_sparse_decode, msa_sparse_decode_select and msa_dense_decode: `scores`
+// null means `topk` is the input list; otherwise the lists are selected from
+// the strided scores inside the attend kernel and written to `topk`.
+// dense_span > 0: no list, every visible block (msa_dense_decode).
 int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
                   const int32_t* seq_lens, const float* scores, int64_t stride_h,
                   int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
                   size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
                   int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
-                  int num_splits, msa_stream_t stream) {
+                  int num_splits, msa_stream_t stream, int dense_span = 0) {
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
-  if (!topk || !out || !aligned(topk, 4) || !aligned(out, 16) || !finite_pos(sm_scale) ||
+  if (dense_span == 0 && (!topk || !aligned(topk, 4))) return MSA_EINVAL;
+  if (!out || !aligned(out, 16) || !finite_pos(sm_scale) ||
       !finite_pos(k_scale) || !std::isfinite(v_scale) || num_splits < 0 ||
       num_splits > kMaxSplits)
     return MSA_EINVAL;
@@ -247,6 +259,7 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   p.s_stride_t = stride_t;
   p.s_stride_n = stride_n;
   p.topk_out = scores ? topk : nullptr;
+  p.dense_span = dense_span;
   p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.part_ml = splits > 1 ? static_cast<float*>(workspace) + splits * rows * MSA_HEAD_DIM : nullptr;
   p.out = static_cast<uint16_t*>(out);
@@ -292,6 +305,25 @@ int msa_sparse_decode_select(const void* q, const void* kv, const int32_t* block
   return sparse_decode(q, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
                        workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
                        k_scale, v_scale, num_splits, stream);
+}
+
+int msa_dense_splits(int S) {
+  if (S < 1) return 0;
+  int nsplit, span;
+  dense_split(S, &nsplit, &span);
+  return span > kDenseMaxSpan ? 0 : nsplit;
+}
+
+int msa_dense_decode(const void* q, const void* kv, const int32_t* block_table,
+                     const int32_t* seq_lens, void* workspace, size_t workspace_bytes, void* out,
+                     int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                     float k_scale, float v_scale, msa_stream_t stream) {
+  if (msa_dense_splits(S) == 0) return MSA_EINVAL;
+  int nsplit, span;
+  dense_split(S, &nsplit, &span);
+  return sparse_decode(q, kv, block_table, seq_lens, nullptr, 0, 0, 0, nullptr, workspace,
+                       workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale, k_scale,
+                       v_scale, nsplit, stream, span);
 }
 
 int msa_get_error(unsigned int* flags, int clear) {

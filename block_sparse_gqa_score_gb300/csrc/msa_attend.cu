@@ -60,6 +60,7 @@ constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it 
 // keys and slots (select mode), stage 2 a copy of the request's block-table
 // row (its first kTableCopy entries; later blocks are read from global memory).
 constexpr int kSelectCap = 8000;              // keys cached (31.25 KiB), then the slots
+constexpr int kMaxPages = 128;                // pages of one CTA (dense decode; a list has 16)
 constexpr int kTableCopy = 512;               // 16 loads per lane, all in flight together
 
 struct AttendTail {
@@ -76,8 +77,8 @@ struct AttendTail {
   uint32_t tmem_base;
   int n_pages, pos;
   float zs;                 // logit scale (log2 units) times 2^e of the query split
-  int pages[kTopK];
-  int blocks[kTopK];
+  int pages[kMaxPages];
+  int blocks[kMaxPages];
 };
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
@@ -99,6 +100,9 @@ __device__ __forceinline__ void fill(float (&a)[N], float v) {
   for (int k = 0; k < N; ++k) a[k] = v;
 }
 
+// kDense: dense decode (every visible block of the CTA's range, no list),
+// compiled separately so that the list modes carry none of its branches.
+template <bool kDense>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap kv_map, const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -145,8 +149,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     // stage 0 before waiting for the previous kernel; a given list without it
     // costs one discarded load.
     const int cur = pos >= 0 ? pos / kPage : -1;
+    // the CTA whose list starts with the current block: split 0 of a list,
+    // the split whose block range holds it in dense decode
+    const int cur_split = kDense ? (cur >= 0 ? cur / p.dense_span : -1) : 0;
     int cur_page = -1;
-    if (cur >= 0 && split == 0) {
+    if (cur >= 0 && split == cur_split) {
       const int pg = cur < ncopy ? table_s[cur] : trow[cur];
       if (pg >= 0 && static_cast<int64_t>(pg) < p.num_blocks) cur_page = pg;
     }
@@ -174,66 +181,106 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(smem + kHalfTile, &kv_map, kHeadDim, row, &tail->full[0]);
       }
     }
-    pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
-    int n;
-    if (p.scores) {
-      // select this row's blocks here; stage 1, not yet loaded, is the scratch
-      bool nan = false;
-      uint8_t* scratch = smem + kStageBytes;
-      n = pos >= 0 ? select::select_row<16>(p.scores + g * p.s_stride_h + i * p.s_stride_t,
-                                        p.s_stride_n, pos, lane,
-                                        reinterpret_cast<uint32_t*>(scratch), kSelectCap,
-                                        reinterpret_cast<int*>(scratch + 4 * kSelectCap), nan)
-                   : -1;
-      if (lane < kTopK) p.topk_out[list + lane] = n;
-      if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);
-    } else {
-      n = lane < kTopK ? p.topk[list + lane] : -1;
-    }
-    int page = -1;
-    bool valid = false;
-    if (lane < kTopK && pos >= 0) {
-      if (n != -1) {
-        if (n < 0 || n > pos / kPage)
-          flag_error(p.err, MSA_ERR_TOPK_RANGE);
-        else
-          valid = true;
+    int np = 0;               // this CTA's pages
+    bool mine_front = false;  // its page 0 is the current block (stage 0 may hold it)
+    if constexpr (kDense) {
+      // dense decode: blocks [lo, hi) of the row, the current block first,
+      // then ascending; nothing here comes from the previous kernel
+      const int lo = split * p.dense_span;
+      const int hi = min(lo + p.dense_span, cur + 1);
+      if (cur >= lo && cur < hi) {
+        if (cur_page >= 0) {
+          if (lane == 0) {
+            tail->pages[0] = cur_page;
+            tail->blocks[0] = cur;
+          }
+          np = 1;
+          mine_front = true;
+        } else if (lane == 0) {
+          flag_error(p.err, MSA_ERR_PAGE_RANGE);
+        }
       }
-    }
-    // a block listed again at a later slot is dropped (a given list only: the
-    // selector's lists hold distinct blocks)
-    const unsigned same = p.scores ? 0u : __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
-    if (valid && (same & ((1u << lane) - 1u))) {
-      flag_error(p.err, MSA_ERR_TOPK_DUP);
-      valid = false;
-    }
-    if (valid) {
-      page = n < ncopy ? table_s[n] : trow[n];
-      if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks) {
-        flag_error(p.err, MSA_ERR_PAGE_RANGE);
+      for (int base = lo; base < hi; base += 32) {
+        const int n = base + lane;
+        bool valid = n < hi && n != cur;
+        int page = -1;
+        if (valid) {
+          page = n < ncopy ? table_s[n] : trow[n];
+          if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks) {
+            flag_error(p.err, MSA_ERR_PAGE_RANGE);
+            valid = false;
+          }
+        }
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+          const int k = np + __popc(vm & ((1u << lane) - 1u));
+          tail->pages[k] = page;
+          tail->blocks[k] = n;
+        }
+        np += __popc(vm);
+      }
+    } else {
+      pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
+      int n;
+      if (p.scores) {
+        // select this row's blocks here; stage 1, not yet loaded, is the scratch
+        bool nan = false;
+        uint8_t* scratch = smem + kStageBytes;
+        n = pos >= 0 ? select::select_row<16>(p.scores + g * p.s_stride_h + i * p.s_stride_t,
+                                          p.s_stride_n, pos, lane,
+                                          reinterpret_cast<uint32_t*>(scratch), kSelectCap,
+                                          reinterpret_cast<int*>(scratch + 4 * kSelectCap), nan)
+                     : -1;
+        if (lane < kTopK) p.topk_out[list + lane] = n;
+        if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(p.err, MSA_ERR_SCORE_NAN);
+      } else {
+        n = lane < kTopK ? p.topk[list + lane] : -1;
+      }
+      int page = -1;
+      bool valid = false;
+      if (lane < kTopK && pos >= 0) {
+        if (n != -1) {
+          if (n < 0 || n > pos / kPage)
+            flag_error(p.err, MSA_ERR_TOPK_RANGE);
+          else
+            valid = true;
+        }
+      }
+      // a block listed again at a later slot is dropped (a given list only: the
+      // selector's lists hold distinct blocks)
+      const unsigned same = p.scores ? 0u : __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
+      if (valid && (same & ((1u << lane) - 1u))) {
+        flag_error(p.err, MSA_ERR_TOPK_DUP);
         valid = false;
       }
-    }
-    // page order: the current block first when listed (in select mode it
-    // always is, and may already be loading), then the others ascending; both
-    // modes use this order, so they give the same bits for the same lists
-    const unsigned vm = __ballot_sync(0xffffffffu, valid);
-    const bool front = valid && n == cur;
-    const unsigned fm = __ballot_sync(0xffffffffu, front);
-    const int idx = front ? 0 : __popc(vm & ((1u << lane) - 1u)) + (fm ? 1 : 0);
-    const bool mine = valid && (idx % p.splits == split);
-    const unsigned mm = __ballot_sync(0xffffffffu, mine);
-    const bool mine_front = (mm & fm) != 0u;
-    if (mine) {
-      const int k = front ? 0 : __popc(mm & ~fm & ((1u << lane) - 1u)) + (mine_front ? 1 : 0);
-      tail->pages[k] = page;
-      tail->blocks[k] = n;
+      if (valid) {
+        page = n < ncopy ? table_s[n] : trow[n];
+        if (page < 0 || static_cast<int64_t>(page) >= p.num_blocks) {
+          flag_error(p.err, MSA_ERR_PAGE_RANGE);
+          valid = false;
+        }
+      }
+      // page order: the current block first when listed (in select mode it
+      // always is, and may already be loading), then the others ascending; both
+      // modes use this order, so they give the same bits for the same lists
+      const unsigned vm = __ballot_sync(0xffffffffu, valid);
+      const bool front = valid && n == cur;
+      const unsigned fm = __ballot_sync(0xffffffffu, front);
+      const int idx = front ? 0 : __popc(vm & ((1u << lane) - 1u)) + (fm ? 1 : 0);
+      const bool mine = valid && (idx % p.splits == split);
+      const unsigned mm = __ballot_sync(0xffffffffu, mine);
+      mine_front = (mm & fm) != 0u;
+      if (mine) {
+        const int k = front ? 0 : __popc(mm & ~fm & ((1u << lane) - 1u)) + (mine_front ? 1 : 0);
+        tail->pages[k] = page;
+        tail->blocks[k] = n;
+      }
+      np = __popc(mm);
     }
     // the scratch writes in stages 1-2 come before the TMA loads into them
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      const int np = __popc(mm);
       tail->n_pages = np;
       tail->pos = pos;
       // stage 0 already holds (or is loading) the current block's page: it is
@@ -535,6 +582,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const int d = key;
       const int64_t row0 = static_cast<int64_t>(i) * p.Hq + g * kGroup;
+      // dense decode waited for no earlier kernel; the outputs (or the split
+      // partials) may still be read by the previous one
+      if constexpr (kDense) pdl_wait();
       if (p.splits == 1) {
 #pragma unroll
         for (int h = 0; h < kGroup; ++h) {
@@ -609,17 +659,23 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   static_assert(kSmemBytes <= 227 * 1024, "attend shared memory");
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    cudaError_t r = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (r != cudaSuccess) return r;
-    // all of the unified L1 / shared storage as shared memory: two CTAs per SM
-    return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    for (auto* k : {attend_kernel<false>, attend_kernel<true>}) {
+      cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (r != cudaSuccess) return r;
+      // all of the unified L1 / shared storage as shared memory: two CTAs per SM
+      r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
   const int T = p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
-  return launch_pdl(attend_kernel, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
+  if (p.dense_span > 0)
+    return launch_pdl(attend_kernel<true>, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
+  return launch_pdl(attend_kernel<false>, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,

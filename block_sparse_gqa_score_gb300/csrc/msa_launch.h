@@ -43,6 +43,9 @@ struct AttendParams {
   const float* scores;
   int64_t s_stride_h, s_stride_t, s_stride_n;
   int32_t* topk_out;
+  // dense decode: > 0 means no list at all; CTA z attends blocks
+  // [z * dense_span, (z + 1) * dense_span) that its token may see
+  int dense_span;
   float* part_o;               // [splits, T, Hq, 128]     (splits > 1)
   float* part_ml;              // [splits, T, Hq, 2]       (splits > 1)
   uint16_t* out;               // bf16 bits [T, Hq, 128]   (splits == 1)

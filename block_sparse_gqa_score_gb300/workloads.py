@@ -43,6 +43,7 @@ class Workload:
     key_outlier_frac: float = 0.0
     key_outlier_mult: float = 1.0
     topk_given: bool = False      # attend-only: draw the top-k list instead of scoring
+    dense: bool = False           # dense decode: every visible block, no scoring or list
     pad_frac: float = 0.0         # fraction of requests with seq_len 0
     seq_args: dict = field(default_factory=dict)
 
@@ -54,7 +55,8 @@ class Workload:
         return {"workload": self.name, "batch": self.batch, "decode_query_len": self.qlen,
                 "num_q_heads": self.num_q_heads, "num_kv_heads": self.num_kv_heads,
                 "head_dim": HEAD_DIM, "page": PAGE, "topk": TOPK, "seq_lens": self.seq_lens,
-                "pipeline": "attend+combine" if self.topk_given else "score+topk+attend+combine"}
+                "pipeline": ("dense attend+combine" if self.dense else "attend+combine"
+                             if self.topk_given else "score+topk+attend+combine")}
 
 
 WORKLOADS = {
@@ -71,6 +73,10 @@ WORKLOADS = {
         Workload("b16_q32_h64kv4_256k_outliers", 16, 32, 64, 4, "fixed", seed=1005,
                  key_outlier_frac=0.05, key_outlier_mult=8.0,
                  seq_args={"values": [262144] * 16}),
+        # the same model's dense layers (every visible block) on the batch-16
+        # decode shapes
+        Workload("dense_b16_q4_h64kv4_8k-32k", 16, 4, 64, 4, "uniform", seed=1006, kv_std=0.5,
+                 kv_scale_mode="amax", dense=True, seq_args={"lo": 8192, "hi": 32768}),
     ]
 }
 
@@ -169,6 +175,23 @@ def draw_topk_given(seq_lens: list[int], qlen: int, hkv: int, gen: torch.Generat
                     pick = torch.randperm(cur, generator=gen)[:TOPK - 1]
                     ids = sorted(pick.tolist()) + [cur]
                 out[b * qlen + j, g, :len(ids)] = torch.tensor(ids, dtype=torch.int32)
+    return out
+
+
+def all_visible_lists(seq_lens: list[int], qlen: int, hkv: int, width: int):
+    """Every visible page ascending, -1 padded to `width` columns: the lists
+    that make the sparse attend dense (any number of pages)."""
+    B = len(seq_lens)
+    out = torch.full((B * qlen, hkv, width), -1, dtype=torch.int32)
+    for b, L in enumerate(seq_lens):
+        for j in range(qlen):
+            visible = L - qlen + j + 1
+            if visible <= 0:
+                continue
+            n = math.ceil(visible / PAGE)
+            if n > width:
+                raise ValueError("more visible pages than columns")
+            out[b * qlen + j, :, :n] = torch.arange(n, dtype=torch.int32)
     return out
 
 

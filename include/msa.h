@@ -11,6 +11,7 @@
  *   msa_sparse_decode  split-K attention over the selected pages (stage 3)
  *   msa_combine        merge of the split-K partials            (stage 4)
  *   msa_sparse_decode_select  stages 2 and 3 in one kernel
+ *   msa_dense_decode   attention over every visible block (dense layers)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -197,6 +198,31 @@ int msa_sparse_decode_select(const void *q, const void *kv, const int32_t *block
                              size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv,
                              int S, int64_t num_blocks, float sm_scale, float k_scale,
                              float v_scale, int num_splits, msa_stream_t stream);
+
+/*
+ * Split count msa_dense_decode uses for a block-table stride of S blocks:
+ * min(16, ceil(S / 16)), each split a range of ceil(S / splits) consecutive
+ * blocks.  Returns 0 when S < 1 or a range would exceed 128 blocks (S > 2048,
+ * contexts beyond 256k tokens), which msa_dense_decode rejects.  Size its
+ * workspace with msa_workspace_bytes(B, Q, Hq, msa_dense_splits(S)).
+ */
+int msa_dense_splits(int S);
+
+/*
+ * msa_dense_decode -- decode attention over every visible block: the dense
+ * layers of the model (the TensorRT-LLM PR #17171 dense-decode commit: the
+ * first layers attend the whole page table).  The same operation as
+ * msa_sparse_decode with each row's list being all of its blocks 0 .. cur(i)
+ * (keys 128 n + t <= pos(i)); no list is read.  Splits as msa_dense_splits;
+ * with more than one the partials go to `workspace` and the merge is enqueued
+ * on `stream`.  Numerics as msa_sparse_decode.
+ * Errors: as msa_sparse_decode (topk and num_splits aside), plus S > 2048
+ * (MSA_EINVAL).  Device: MSA_ERR_PAGE_RANGE (page skipped), MSA_ERR_SEQ_RANGE.
+ */
+int msa_dense_decode(const void *q, const void *kv, const int32_t *block_table,
+                     const int32_t *seq_lens, void *workspace, size_t workspace_bytes, void *out,
+                     int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                     float k_scale, float v_scale, msa_stream_t stream);
 
 /*
  * msa_combine -- stage 4, merge of split-K partials ("fp32 split-K partials"

@@ -148,3 +148,32 @@ def test_valid_call_without_a_device_fails_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a device is present")
     assert _score(lib) == _native.ECUDA
+
+
+def test_dense_splits_rule(lib):
+    # min(16, ceil(S / 16)) splits of ceil(S / splits) blocks; ranges over 128
+    # blocks (S > 2048) are not taken
+    assert lib.msa_dense_splits(0) == 0
+    assert lib.msa_dense_splits(1) == 1
+    assert lib.msa_dense_splits(16) == 1
+    assert lib.msa_dense_splits(17) == 2
+    assert lib.msa_dense_splits(255) == 16
+    assert lib.msa_dense_splits(2048) == 16
+    assert lib.msa_dense_splits(2049) == 0
+
+
+def test_dense_decode_rejects(lib):
+    f = lib.msa_dense_decode
+    ok = dict(q=A, kv=A, bt=A, sl=A, ws=A, wsb=1 << 30, out=A, B=16, Q=4, Hq=64, Hkv=4, S=8,
+              NB=100, sm=0.088, ks=1.0, vs=1.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["kv"], a["bt"], a["sl"], a["ws"], a["wsb"], a["out"], a["B"], a["Q"],
+                 a["Hq"], a["Hkv"], a["S"], a["NB"], a["sm"], a["ks"], a["vs"], None)
+
+    assert call(S=2049) == EINVAL                   # a split would span more than 128 blocks
+    assert call(out=None) == EINVAL
+    assert call(Q=33) == EINVAL
+    assert call(vs=float("nan")) == EINVAL
+    assert call(B=0) == 0                           # empty batch

@@ -269,3 +269,70 @@ def test_attend_lists_without_the_current_block():
         ref = oracle.attend(to_problem(inp, oracle), topk.numpy())
         assert_out_close(_np(out), ref, padding_rows(seq_lens, Q))
         assert msa.get_error() == 0
+
+
+DENSE_CASES = [
+    ([2048, 3000], 1, 16, 1),                     # the tiny workload's shapes
+    ([129, 385, 0, 7], 4, 64, 4),                 # one split, padding rows
+    ([0, 2, 3, 130, 2048, 2049], 4, 16, 1),       # page boundaries
+    ([2500, 700], 32, 16, 1),                     # qlen at its upper bound
+    ([20000, 9000, 40000], 4, 64, 4),             # 16 splits of 20 blocks
+    ([70000], 2, 16, 1),                          # blocks past the prologue's table copy
+]
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", DENSE_CASES)
+def test_dense_decode_matches_oracle(seq_lens, Q, Hq, Hkv):
+    """Dense decode against the oracle's attend over every visible block."""
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=110, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    out = msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                           inp.k_scale, inp.v_scale)
+    lists = wl.all_visible_lists(seq_lens, Q, Hkv, inp.stride)
+    ref = oracle.attend(to_problem(inp, oracle), lists.numpy())
+    assert_out_close(_np(out), ref, padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
+
+
+def test_dense_decode_equals_sparse_decode_on_short_rows():
+    """With at most 16 visible blocks per row, dense decode and the sparse
+    attend over all-visible lists take the same pages in the same order: the
+    same bits."""
+    seq_lens, Q, Hq, Hkv = [257, 513, 2048, 1, 0], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=111, device=DEV, kv_std=0.5)
+    dense = msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                             inp.k_scale, inp.v_scale)
+    topk = wl.all_visible_topk(seq_lens, Q, Hkv).to(DEV)
+    sparse = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, Q,
+                               inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=1)
+    assert torch.equal(dense, sparse)
+    assert msa.get_error() == 0
+
+
+def test_dense_decode_graph_replay_after_lengths_change():
+    """Captured once, replayed after seq_lens change (split count fixed by the
+    table's stride): still the oracle's result."""
+    Q, Hq, Hkv = 2, 32, 2
+    lens_a, lens_b = [9000, 3000, 12000], [4000, 12800, 130]
+    inp = wl.make_custom(lens_a, Q, Hq, Hkv, seed=112, device=DEV, kv_std=0.5, min_stride=100)
+    out = torch.empty_like(inp.q)
+    ws = torch.empty(msa.workspace_bytes(3, Q, Hq, msa.dense_splits(inp.stride)) or 1,
+                     dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                         inp.k_scale, inp.v_scale, out=out, workspace=ws)
+        with torch.cuda.graph(graph, stream=s):
+            msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                             inp.k_scale, inp.v_scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    inp.seq_lens.copy_(torch.tensor(lens_b, dtype=torch.int32))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = oracle.attend(to_problem(inp, oracle),
+                        wl.all_visible_lists(lens_b, Q, Hkv, inp.stride).numpy())
+    assert_out_close(_np(out), ref, padding_rows(lens_b, Q))
+    assert msa.get_error() == 0

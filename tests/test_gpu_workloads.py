@@ -42,7 +42,12 @@ def test_workload_full_size_sampled(name):
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     msa.get_error(clear=True)
     p = to_problem(inp, oracle)
-    if w.topk_given:
+    if w.dense:
+        # every visible block: the oracle attends over all-visible lists
+        topk = wl.all_visible_lists(inp.seq_lens_list, inp.qlen, inp.num_kv_heads, inp.stride)
+        out = msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
+                               inp.sm_scale, inp.k_scale, inp.v_scale)
+    elif w.topk_given:
         topk = inp.topk
         out = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, inp.qlen,
                                 inp.sm_scale, inp.k_scale, inp.v_scale)
