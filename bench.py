@@ -618,10 +618,8 @@ def run_ours(args, rank, world, local):
         line["e2e"] = _e2e(msa, w, layers, bufs, stream, dev, world, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp0 = layers[0]
-        lists = _given_lists(w, inp0)
-        if lists is None:   # the step's own selection
-            lists = bufs[0].topk.cpu().numpy()
-        line["cpu_baseline"] = cpu_baseline(_to_cpu(inp0), w, lists)
+        # None (a scoring workload): the oracle scores and selects as well
+        line["cpu_baseline"] = cpu_baseline(_to_cpu(inp0), w, _given_lists(w, inp0))
     if rank == 0:
         print(json.dumps(line))
 
