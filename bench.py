@@ -230,7 +230,8 @@ def _work(inp, topk_cpu: np.ndarray | None, reads_lists: bool = True):
     B, Q, Hq, Hkv, S = inp.batch, inp.qlen, inp.num_q_heads, inp.num_kv_heads, inp.stride
     T = B * Q
     pages = [math.ceil(L / 128) for L in inp.seq_lens_list]
-    q_bytes = T * Hq * 128 * 2
+    q_bytes = T * Hq * 128 * inp.q.element_size()   # bf16, or an fp8 query
+    out_bytes = T * Hq * 128 * 2
     score = sum(pages) * Hkv * 16384 + q_bytes + Hkv * T * S * 4 + B * S * 4
     cand = 0
     for b, L in enumerate(inp.seq_lens_list):
@@ -252,7 +253,7 @@ def _work(inp, topk_cpu: np.ndarray | None, reads_lists: bool = True):
                 ids = ids[ids >= 0]
                 union += len(np.unique(ids))
                 per_token += len(ids)
-    attend = union * 32768 + 2 * q_bytes + (T * Hkv * 16 * 4 if reads_lists else 0)
+    attend = union * 32768 + q_bytes + out_bytes + (T * Hkv * 16 * 4 if reads_lists else 0)
     return {"score": score, "topk": topk, "attend": attend, "union_pages": union,
             "token_pages": per_token, "attend_kv_bytes": union * 32768, "score_flops": score_flops}
 
@@ -316,10 +317,14 @@ def _given_lists(w, inp):
 
 
 def _problem(inp, oracle):
-    return oracle.Problem(inp.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16),
+    # an fp8 query (value q * q_scale): its codes as bf16 (exact) with sm_scale * q_scale
+    q, sm_scale = inp.q, inp.sm_scale
+    if q.dtype != torch.bfloat16:
+        q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
+    return oracle.Problem(q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16),
                           inp.kv.cpu().numpy(), inp.block_table.cpu().numpy(),
                           inp.seq_lens.cpu().numpy(), inp.qlen, inp.num_q_heads,
-                          inp.num_kv_heads, inp.sm_scale, inp.k_scale, inp.v_scale)
+                          inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
 
 
 def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
@@ -399,15 +404,17 @@ def run_ours(args, rank, world, local):
             return [lambda: None, lambda: None,
                     lambda: msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
                                              inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
-                                             out=bf.out, workspace=bf.workspace)]
+                                             out=bf.out, workspace=bf.workspace,
+                                             q_scale=inp.q_scale)]
         if w.topk_given:
             return [lambda: None, lambda: None,
                     lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
                                               inp.topk, inp.qlen, inp.sm_scale, inp.k_scale,
                                               inp.v_scale, out=bf.out, num_splits=bf.num_splits,
-                                              workspace=bf.workspace)]
+                                              workspace=bf.workspace, q_scale=inp.q_scale)]
         score_call = lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
-                                       inp.sm_scale, inp.k_scale, scores=bf.scores)
+                                       inp.sm_scale, inp.k_scale, scores=bf.scores,
+                                       q_scale=inp.q_scale)
         if fused:   # the selection runs inside the attend kernel (msa_sparse_decode_select)
             return [score_call, lambda: None,
                     lambda: msa.sparse_decode_select(inp.q, inp.kv, inp.block_table,
@@ -415,13 +422,14 @@ def run_ours(args, rank, world, local):
                                                      inp.sm_scale, inp.k_scale, inp.v_scale,
                                                      topk_out=bf.topk, out=bf.out,
                                                      num_splits=bf.num_splits,
-                                                     workspace=bf.workspace)]
+                                                     workspace=bf.workspace,
+                                                     q_scale=inp.q_scale)]
         return [score_call,
                 lambda: msa.topk(bf.scores, inp.seq_lens, inp.qlen, out=bf.topk),
                 lambda: msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk,
                                           inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
                                           out=bf.out, num_splits=bf.num_splits,
-                                          workspace=bf.workspace)]
+                                          workspace=bf.workspace, q_scale=inp.q_scale)]
 
     attend_only = w.topk_given or w.dense
     fused = (not attend_only) and msa.fused_selection(first.stride)
@@ -530,7 +538,8 @@ def run_ours(args, rank, world, local):
             inp, bf = layers[l], bufs[l]
             msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, bf.topk, inp.qlen,
                               inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
-                              num_splits=bf.num_splits, workspace=bf.workspace)
+                              num_splits=bf.num_splits, workspace=bf.workspace,
+                              q_scale=inp.q_scale)
         g = None
         if graphs:
             g = torch.cuda.CUDAGraph()
@@ -685,14 +694,16 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
         if w.topk_given:
             msa.sparse_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], v["topk"],
                               inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
-                              num_splits=bf.num_splits, workspace=bf.workspace)
+                              num_splits=bf.num_splits, workspace=bf.workspace,
+                              q_scale=inp.q_scale)
         elif w.dense:
             msa.dense_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
                              inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
-                             workspace=bf.workspace)
+                             workspace=bf.workspace, q_scale=inp.q_scale)
         else:
             msa.decode_step(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
-                            inp.sm_scale, inp.k_scale, inp.v_scale, buffers=bf)
+                            inp.sm_scale, inp.k_scale, inp.v_scale, buffers=bf,
+                            q_scale=inp.q_scale)
 
     def d2h(k):
         l = k % n_layers

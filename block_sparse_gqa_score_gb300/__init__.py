@@ -21,6 +21,7 @@ seq_lens int32 [B]; scores fp32 [Hkv, T, S]; topk int32 [T, Hkv, 16].
 from __future__ import annotations
 
 import ctypes
+import math
 from dataclasses import dataclass
 
 import torch
@@ -65,8 +66,11 @@ def _need(t: torch.Tensor, name: str, dtypes, device=None):
 _KV_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 
 
+_FP8_Q = getattr(torch, "float8_e4m3fn", None)
+
+
 def _geometry(q, kv, block_table, seq_lens, qlen):
-    _need(q, "q", (torch.bfloat16,))
+    _need(q, "q", (torch.bfloat16,) + ((_FP8_Q,) if _FP8_Q is not None else ()))
     dev = q.device
     _need(kv, "kv", _KV_DTYPES, dev)
     _need(block_table, "block_table", (torch.int32,), dev)
@@ -95,18 +99,31 @@ def choose_splits(batch: int, qlen: int, num_kv_heads: int, sm_count: int | None
     return int(_lib().msa_choose_splits(batch, qlen, num_kv_heads, sm_count))
 
 
+def _fp8(q, q_scale: float) -> bool:
+    """Whether q is an fp8 query (then its value is q * q_scale)."""
+    if q.dtype == torch.bfloat16:
+        return False
+    if not (q_scale > 0 and math.isfinite(q_scale)):
+        raise ValueError("an fp8 query needs a finite q_scale > 0")
+    return True
+
+
 def score(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
-          scores: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Block scores fp32 [Hkv, T, S] (msa_score)."""
+          scores: torch.Tensor | None = None, stream=None, q_scale: float = 1.0) -> torch.Tensor:
+    """Block scores fp32 [Hkv, T, S] (msa_score; msa_score_q8 for an fp8 q of
+    value q * q_scale)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if scores is None:
         scores = torch.empty((Hkv, B * qlen, S), dtype=torch.float32, device=dev)
     _need(scores, "scores", (torch.float32,), dev)
     if tuple(scores.shape) != (Hkv, B * qlen, S):
         raise ValueError("scores must be [Hkv, T, S]")
-    st = _lib().msa_score(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
-                          scores.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
-                          float(k_scale), _stream(dev, stream))
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), scores.data_ptr(), B, qlen,
+            Hq, Hkv, S, NB, float(sm_scale), float(k_scale), _stream(dev, stream))
+    if _fp8(q, q_scale):
+        st = _lib().msa_score_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        st = _lib().msa_score(q.data_ptr(), *args)
     _native.check(st, "msa_score")
     return scores
 
@@ -136,7 +153,7 @@ def topk(scores: torch.Tensor, seq_lens: torch.Tensor, qlen: int, k: int = TOPK,
 def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: float,
                   k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
                   num_splits: int = 0, workspace: torch.Tensor | None = None,
-                  stream=None) -> torch.Tensor:
+                  stream=None, q_scale: float = 1.0) -> torch.Tensor:
     """Attention over the selected pages, bf16 [T, Hq, 128] (msa_sparse_decode;
     with more than one split the merge runs on the same stream)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
@@ -144,7 +161,7 @@ def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: f
     if tuple(topk_idx.shape) != (B * qlen, Hkv, TOPK):
         raise ValueError("topk must be [T, Hkv, 16]")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev)
     splits = num_splits if num_splits > 0 else choose_splits(B, qlen, Hkv)
     need = workspace_bytes(B, qlen, Hq, splits)
@@ -152,10 +169,13 @@ def sparse_decode(q, kv, block_table, seq_lens, topk_idx, qlen: int, sm_scale: f
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = _lib().msa_sparse_decode(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(),
-                                  seq_lens.data_ptr(), topk_idx.data_ptr(), ws_ptr, ws_bytes,
-                                  out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
-                                  float(k_scale), float(v_scale), splits, _stream(dev, stream))
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), topk_idx.data_ptr(), ws_ptr,
+            ws_bytes, out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale), float(k_scale),
+            float(v_scale), splits, _stream(dev, stream))
+    if _fp8(q, q_scale):
+        st = _lib().msa_sparse_decode_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        st = _lib().msa_sparse_decode(q.data_ptr(), *args)
     _native.check(st, "msa_sparse_decode")
     return out
 
@@ -168,12 +188,13 @@ def dense_splits(stride: int) -> int:
 
 def dense_decode(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
                  v_scale: float = 1.0, out: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                 workspace: torch.Tensor | None = None, stream=None,
+                 q_scale: float = 1.0) -> torch.Tensor:
     """Attention over every visible block, bf16 [T, Hq, 128] (msa_dense_decode;
     with more than one split the merge runs on the same stream)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev)
     splits = dense_splits(S)
     if splits == 0:
@@ -183,10 +204,13 @@ def dense_decode(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_sca
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = _lib().msa_dense_decode(q.data_ptr(), kv.data_ptr(), block_table.data_ptr(),
-                                 seq_lens.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B, qlen, Hq,
-                                 Hkv, S, NB, float(sm_scale), float(k_scale), float(v_scale),
-                                 _stream(dev, stream))
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), ws_ptr, ws_bytes,
+            out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale), float(k_scale),
+            float(v_scale), _stream(dev, stream))
+    if _fp8(q, q_scale):
+        st = _lib().msa_dense_decode_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        st = _lib().msa_dense_decode(q.data_ptr(), *args)
     _native.check(st, "msa_dense_decode")
     return out
 
@@ -207,7 +231,7 @@ def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_sca
                          k_scale: float = 1.0, v_scale: float = 1.0,
                          topk_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
                          num_splits: int = 0, workspace: torch.Tensor | None = None,
-                         stream=None):
+                         stream=None, q_scale: float = 1.0):
     """Selection and attention in one kernel (msa_sparse_decode_select): the
     top-16 blocks of every (token, KV head) row are selected from `scores`
     (any strides, as msa_topk) and attended.  Returns (topk [T, Hkv, 16], out)."""
@@ -223,7 +247,7 @@ def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_sca
         topk_out = torch.empty((B * qlen, Hkv, TOPK), dtype=torch.int32, device=dev)
     _need(topk_out, "topk_out", (torch.int32,), dev)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev)
     splits = num_splits if num_splits > 0 else choose_splits(B, qlen, Hkv)
     need = workspace_bytes(B, qlen, Hq, splits)
@@ -232,11 +256,13 @@ def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_sca
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     sh, st, sn = scores.stride()
-    status = _lib().msa_sparse_decode_select(
-        q.data_ptr(), kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
-        scores.data_ptr(), sh, st, sn, topk_out.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B,
-        qlen, Hq, Hkv, S, NB, float(sm_scale), float(k_scale), float(v_scale), splits,
-        _stream(dev, stream))
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), scores.data_ptr(), sh, st,
+            sn, topk_out.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B, qlen, Hq, Hkv, S, NB,
+            float(sm_scale), float(k_scale), float(v_scale), splits, _stream(dev, stream))
+    if _fp8(q, q_scale):
+        status = _lib().msa_sparse_decode_select_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        status = _lib().msa_sparse_decode_select(q.data_ptr(), *args)
     _native.check(status, "msa_sparse_decode_select")
     return topk_out, out
 
@@ -281,7 +307,8 @@ class DecodeBuffers:
 
 
 def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
-                v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None):
+                v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None,
+                q_scale: float = 1.0):
     """score, then selection + attention on one stream, no host sync: in one
     kernel (msa_sparse_decode_select) while rows have at most FUSED_MAX_BLOCKS
     candidate blocks, else msa_topk then msa_sparse_decode (-> combine when
@@ -290,17 +317,17 @@ def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scal
     if buffers is None:
         buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
     score(q, kv, block_table, seq_lens, qlen, sm_scale, k_scale, scores=buffers.scores,
-          stream=stream)
+          stream=stream, q_scale=q_scale)
     if fused_selection(S):
         sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale,
                              k_scale, v_scale, topk_out=buffers.topk, out=buffers.out,
                              num_splits=buffers.num_splits, workspace=buffers.workspace,
-                             stream=stream)
+                             stream=stream, q_scale=q_scale)
     else:
         topk(buffers.scores, seq_lens, qlen, out=buffers.topk, stream=stream)
         sparse_decode(q, kv, block_table, seq_lens, buffers.topk, qlen, sm_scale, k_scale,
                       v_scale, out=buffers.out, num_splits=buffers.num_splits,
-                      workspace=buffers.workspace, stream=stream)
+                      workspace=buffers.workspace, stream=stream, q_scale=q_scale)
     return buffers.scores, buffers.topk, buffers.out
 
 

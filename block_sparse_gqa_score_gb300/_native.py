@@ -21,7 +21,8 @@ ERR_TIMEOUT = 0x20
 EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode", "msa_combine", "msa_get_error", "msa_strerror", "msa_version",
            "msa_sparse_decode_static", "msa_sparse_decode_select", "msa_dense_splits",
-           "msa_dense_decode")
+           "msa_dense_decode", "msa_score_q8", "msa_sparse_decode_q8",
+           "msa_sparse_decode_select_q8", "msa_dense_decode_q8")
 
 _lib = None
 _lock = threading.Lock()
@@ -66,12 +67,20 @@ def load(path: str | None = None):
         lib.msa_dense_splits.argtypes = [i32]
         lib.msa_dense_decode.argtypes = [P, P, P, P, P, sz, P, i32, i32, i32, i32, i32, i64, f32,
                                          f32, f32, P]
+        # the fp8-query variants: (q8, q_scale) in place of q
+        lib.msa_score_q8.argtypes = [P, f32] + lib.msa_score.argtypes[1:]
+        lib.msa_sparse_decode_q8.argtypes = [P, f32] + lib.msa_sparse_decode.argtypes[1:]
+        lib.msa_sparse_decode_select_q8.argtypes = ([P, f32] +
+                                                    lib.msa_sparse_decode_select.argtypes[1:])
+        lib.msa_dense_decode_q8.argtypes = [P, f32] + lib.msa_dense_decode.argtypes[1:]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
         for name in ("msa_score", "msa_topk", "msa_choose_splits", "msa_sparse_decode",
                      "msa_combine", "msa_get_error", "msa_version", "msa_sparse_decode_static",
-                     "msa_sparse_decode_select", "msa_dense_splits", "msa_dense_decode"):
+                     "msa_sparse_decode_select", "msa_dense_splits", "msa_dense_decode",
+                     "msa_score_q8", "msa_sparse_decode_q8", "msa_sparse_decode_select_q8",
+                     "msa_dense_decode_q8"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -138,12 +138,18 @@ int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
   return static_cast<int>(s < 1 ? 1 : s);
 }
 
-int msa_score(const void* q, const void* kv, const int32_t* block_table, const int32_t* seq_lens,
-              float* scores, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
-              float sm_scale, float k_scale, msa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// msa_score and msa_score_q8: q_scale > 0 means q is fp8 e4m3 (value q * q_scale).
+int score(const void* q, float q_scale, const void* kv, const int32_t* block_table,
+          const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
+          int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream) {
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
-  if (!scores || !aligned(scores, 4) || !finite_pos(sm_scale) || !finite_pos(k_scale))
+  if (!scores || !aligned(scores, 4) || !finite_pos(sm_scale) || !finite_pos(k_scale) ||
+      !(q_scale == 0.f || finite_pos(q_scale)))
     return MSA_EINVAL;
   if (B == 0) return MSA_OK;
   DeviceState* dev;
@@ -151,7 +157,9 @@ int msa_score(const void* q, const void* kv, const int32_t* block_table, const i
   CUtensorMap map;
   if ((st = encode_kv_map(kv, Hkv, num_blocks, &map, /*l2_256=*/false)) != MSA_OK) return st;
   msa::ScoreParams p{};
-  p.q = static_cast<const uint16_t*>(q);
+  p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
+  p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
+  p.q_scale = q_scale;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.scores = scores;
@@ -165,6 +173,25 @@ int msa_score(const void* q, const void* kv, const int32_t* block_table, const i
   p.num_blocks = num_blocks;
   p.scale = sm_scale * k_scale;
   return from_cuda(msa::launch_score(map, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int msa_score(const void* q, const void* kv, const int32_t* block_table, const int32_t* seq_lens,
+              float* scores, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
+              float sm_scale, float k_scale, msa_stream_t stream) {
+  return score(q, 0.f, kv, block_table, seq_lens, scores, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+               k_scale, stream);
+}
+
+int msa_score_q8(const void* q8, float q_scale, const void* kv, const int32_t* block_table,
+                 const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
+                 int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream) {
+  if (!finite_pos(q_scale)) return MSA_EINVAL;
+  return score(q8, q_scale, kv, block_table, seq_lens, scores, B, Q, Hq, Hkv, S, num_blocks,
+               sm_scale, k_scale, stream);
 }
 
 int msa_topk(const float* scores, int64_t stride_h, int64_t stride_t, int64_t stride_n,
@@ -229,7 +256,8 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
                   int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
                   size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
                   int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
-                  int num_splits, msa_stream_t stream, int dense_span = 0) {
+                  int num_splits, msa_stream_t stream, int dense_span = 0, float q_scale = 0.f) {
+  if (!(q_scale == 0.f || finite_pos(q_scale))) return MSA_EINVAL;
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
   if (dense_span == 0 && (!topk || !aligned(topk, 4))) return MSA_EINVAL;
@@ -250,7 +278,9 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
   const int64_t rows = static_cast<int64_t>(B) * Q * Hq;
   msa::AttendParams p{};
-  p.q = static_cast<const uint16_t*>(q);
+  p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
+  p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
+  p.q_scale = q_scale;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.topk = topk;
@@ -307,6 +337,32 @@ int msa_sparse_decode_select(const void* q, const void* kv, const int32_t* block
                        k_scale, v_scale, num_splits, stream);
 }
 
+// The fp8-query variants: q8 is fp8 e4m3 [T, Hq, 128] whose value is q8 *
+// q_scale; everything else as the bf16 entry points.
+int msa_sparse_decode_q8(const void* q8, float q_scale, const void* kv,
+                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk,
+                         void* workspace, size_t workspace_bytes, void* out, int B, int Q, int Hq,
+                         int Hkv, int S, int64_t num_blocks, float sm_scale, float k_scale,
+                         float v_scale, int num_splits, msa_stream_t stream) {
+  if (!finite_pos(q_scale)) return MSA_EINVAL;
+  return sparse_decode(q8, kv, block_table, seq_lens, nullptr, 0, 0, 0, const_cast<int32_t*>(topk),
+                       workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, q_scale);
+}
+
+int msa_sparse_decode_select_q8(const void* q8, float q_scale, const void* kv,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const float* scores, int64_t stride_h, int64_t stride_t,
+                                int64_t stride_n, int32_t* topk, void* workspace,
+                                size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv,
+                                int S, int64_t num_blocks, float sm_scale, float k_scale,
+                                float v_scale, int num_splits, msa_stream_t stream) {
+  if (!finite_pos(q_scale) || !scores) return MSA_EINVAL;
+  return sparse_decode(q8, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
+                       workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, q_scale);
+}
+
 int msa_dense_splits(int S) {
   if (S < 1) return 0;
   int nsplit, span;
@@ -324,6 +380,19 @@ int msa_dense_decode(const void* q, const void* kv, const int32_t* block_table,
   return sparse_decode(q, kv, block_table, seq_lens, nullptr, 0, 0, 0, nullptr, workspace,
                        workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale, k_scale,
                        v_scale, nsplit, stream, span);
+}
+
+int msa_dense_decode_q8(const void* q8, float q_scale, const void* kv,
+                        const int32_t* block_table, const int32_t* seq_lens, void* workspace,
+                        size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                        int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                        msa_stream_t stream) {
+  if (msa_dense_splits(S) == 0 || !finite_pos(q_scale)) return MSA_EINVAL;
+  int nsplit, span;
+  dense_split(S, &nsplit, &span);
+  return sparse_decode(q8, kv, block_table, seq_lens, nullptr, 0, 0, 0, nullptr, workspace,
+                       workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale, k_scale,
+                       v_scale, nsplit, stream, span, q_scale);
 }
 
 int msa_get_error(unsigned int* flags, int clear) {

@@ -100,9 +100,10 @@ __device__ __forceinline__ void fill(float (&a)[N], float v) {
   for (int k = 0; k < N; ++k) a[k] = v;
 }
 
-// kDense: dense decode (every visible block of the CTA's range, no list),
-// compiled separately so that the list modes carry none of its branches.
-template <bool kDense>
+// kDense: dense decode (every visible block of the CTA's range, no list);
+// kFp8Q: an fp8 query (q8 * q_scale).  Each is compiled separately so that the
+// bf16 list-mode kernel carries none of their branches.
+template <bool kDense, bool kFp8Q>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap kv_map, const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -305,10 +306,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::tmem_alloc(&tail->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   } else if (warp == kSoftmaxWarp0) {
-    const int e = prepare_query_e4m3(p.q + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim,
-                                     0, qhi, qlo, lane);
+    const int64_t row = static_cast<int64_t>(i) * p.Hq + g * kGroup;
+    if constexpr (kFp8Q) {  // fp8 query as stored; the lo rows of the product are zero
+      store_query_rows_fp8(p.q8 + row * kHeadDim, 0, qhi, lane);
+      zero_query_rows(0, qlo, lane);
+      if (lane == 0) tail->zs = p.logit_scale * p.q_scale;
+    } else {
+      const int e = prepare_query_e4m3(p.q + row * kHeadDim, 0, qhi, qlo, lane);
+      if (lane == 0) tail->zs = p.logit_scale * exp2i(e);
+    }
     tc::fence_proxy_async_smem();  // the tiles are read by the tensor core
-    if (lane == 0) tail->zs = p.logit_scale * exp2i(e);
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -659,7 +666,8 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   static_assert(kSmemBytes <= 227 * 1024, "attend shared memory");
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    for (auto* k : {attend_kernel<false>, attend_kernel<true>}) {
+    for (auto* k : {attend_kernel<false, false>, attend_kernel<true, false>,
+                    attend_kernel<false, true>, attend_kernel<true, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (r != cudaSuccess) return r;
@@ -673,9 +681,14 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   if (e != cudaSuccess) return e;
   const int T = p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
-  if (p.dense_span > 0)
-    return launch_pdl(attend_kernel<true>, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
-  return launch_pdl(attend_kernel<false>, grid, dim3(kThreads), kSmemBytes, stream, kv_map, p);
+  const dim3 block(kThreads);
+  if (p.q8)
+    return p.dense_span > 0
+               ? launch_pdl(attend_kernel<true, true>, grid, block, kSmemBytes, stream, kv_map, p)
+               : launch_pdl(attend_kernel<false, true>, grid, block, kSmemBytes, stream, kv_map, p);
+  return p.dense_span > 0
+             ? launch_pdl(attend_kernel<true, false>, grid, block, kSmemBytes, stream, kv_map, p)
+             : launch_pdl(attend_kernel<false, false>, grid, block, kSmemBytes, stream, kv_map, p);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,

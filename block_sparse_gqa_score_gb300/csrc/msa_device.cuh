@@ -303,6 +303,29 @@ __device__ __forceinline__ int store_query_e4m3(const uint4 (&raw)[8], int row0,
   return e;
 }
 
+// An fp8 e4m3 query token's 16 rows (16 heads x 128 B, contiguous) copied as
+// stored into rows row0 .. row0 + 15 of a 128B-swizzled K-major tile; lane l
+// moves 64 bytes of row l / 2.
+__device__ __forceinline__ void store_query_rows_fp8(const uint8_t* __restrict__ rows, int row0,
+                                                     uint8_t* tile, int lane) {
+  const int r = lane >> 1, half = lane & 1;
+  const uint4* src = reinterpret_cast<const uint4*>(rows + r * 128 + 64 * half);
+  uint4 v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(tile + sw128(row0 + r, 4 * half + k)) = v[k];
+}
+
+// Rows row0 .. row0 + 15 of a 128B-swizzled tile set to zero (lane l: 64
+// bytes of row l / 2).
+__device__ __forceinline__ void zero_query_rows(int row0, uint8_t* tile, int lane) {
+  const int r = lane >> 1, half = lane & 1;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(tile + sw128(row0 + r, 4 * half + k)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
 __device__ __forceinline__ int prepare_query_e4m3(const uint16_t* __restrict__ rows, int row0,
                                                   uint8_t* hi, uint8_t* lo, int lane) {
   uint4 raw[8];

@@ -12,7 +12,7 @@
 namespace msa {
 
 struct ScoreParams {
-  const uint16_t* q;           // bf16 bits [T, Hq, 128]
+  const uint16_t* q;           // bf16 bits [T, Hq, 128] (when q8 is null)
   const int32_t* block_table;  // [B, S]
   const int32_t* seq_lens;     // [B]
   float* scores;               // [Hkv, T, S]
@@ -21,6 +21,8 @@ struct ScoreParams {
   int ctas;                    // SM count (the scorer runs one or two CTAs per SM)
   int64_t num_blocks;
   float scale;                 // sm_scale * k_scale
+  const uint8_t* q8;           // fp8 e4m3 [T, Hq, 128], value q8 * q_scale; or nullptr
+  float q_scale;
 };
 
 struct TopkParams {
@@ -33,7 +35,7 @@ struct TopkParams {
 };
 
 struct AttendParams {
-  const uint16_t* q;           // bf16 bits [T, Hq, 128]
+  const uint16_t* q;           // bf16 bits [T, Hq, 128] (when q8 is null)
   const int32_t* block_table;  // [B, S]
   const int32_t* seq_lens;     // [B]
   const int32_t* topk;         // [T, Hkv, 16]; unused when `scores` is given
@@ -54,6 +56,8 @@ struct AttendParams {
   int64_t num_blocks;
   float logit_scale;           // sm_scale * k_scale * log2(e)
   float v_scale;
+  const uint8_t* q8;           // fp8 e4m3 [T, Hq, 128], value q8 * q_scale; or nullptr
+  float q_scale;
 };
 
 // Runs `set_up` once per device (e.g. raising a kernel's dynamic shared-memory

@@ -167,18 +167,29 @@ __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk&
 }
 
 // Query tile of unit (b, g) into hi / lo (16 Q rows x 128 B each, 128B
-// swizzled, K-major), per-token factors scale * 2^e into qmul[0..Q).
+// swizzled, K-major), per-token factors into qmul[0..Q): a bf16 query scaled
+// by 2^-e and split exactly into hi + lo (factor scale * 2^e), or an fp8 query
+// as stored in hi (lo unused; factor scale * q_scale).
+template <bool kFp8Q>
 __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
                                    float* qmul, int lane) {
   for (int jq = 0; jq < p.Q; ++jq) {
-    const uint16_t* rows = p.q + ((static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup) * kHeadDim;
-    const int e = prepare_query_e4m3(rows, jq * kGroup, qhi, qlo, lane);
-    if (lane == 0) qmul[jq] = p.scale * exp2i(e);
+    const int64_t row = (static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup;
+    if constexpr (kFp8Q) {
+      store_query_rows_fp8(p.q8 + row * kHeadDim, jq * kGroup, qhi, lane);
+      if (lane == 0) qmul[jq] = p.scale * p.q_scale;
+    } else {
+      const int e = prepare_query_e4m3(p.q + row * kHeadDim, jq * kGroup, qhi, qlo, lane);
+      if (lane == 0) qmul[jq] = p.scale * exp2i(e);
+    }
   }
 }
 
 // At most 128 registers: registers are allocated per SM sub-partition (16K
-// each), so two 7-warp CTAs per SM need <= 128 per thread.
+// each), so two 7-warp CTAs per SM need <= 128 per thread.  kFp8Q: the query
+// is fp8 (q8 * q_scale), compiled separately so that the bf16 kernel carries
+// none of its branches.
+template <bool kFp8Q>
 __global__ void __maxnreg__(128)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -374,9 +385,11 @@ __global__ void __maxnreg__(128)
           const uint64_t bh = bq + static_cast<uint64_t>((h * G.Qu * kGroup * 128) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bh + 2 * ks, idesc[h], ks > 0);
+          if constexpr (!kFp8Q) {  // the lo part of a bf16 query adds into the same columns
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
+          }
           tc::commit(&tail->dfull[buf]);
         }
         tc::commit(&tail->empty[s]);
@@ -404,7 +417,7 @@ __global__ void __maxnreg__(128)
       }
       uint8_t* qhi = qtiles + qb * G.qtile_bytes;
       float* qmul = qmul_ring + (k % kQmulRing) * Q;
-      prepare_query_tile(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane);
+      prepare_query_tile<kFp8Q>(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane);
       tc::fence_proxy_async_smem();   // the tile is read by the tensor core
       __syncwarp();
       if (lane == 0) {
@@ -558,17 +571,23 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    cudaError_t r = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemLimit);
-    if (r != cudaSuccess) return r;
-    // all of the unified L1 / shared storage as shared memory, so that two
-    // CTAs of ~100 KB can be resident on one SM
-    return cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    for (auto* k : {score_kernel<false>, score_kernel<true>}) {
+      cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemLimit);
+      if (r != cudaSuccess) return r;
+      // all of the unified L1 / shared storage as shared memory, so that two
+      // CTAs of ~100 KB can be resident on one SM
+      r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(score_kernel, dim3(p.ctas * G.per_sm), dim3(kThreads), G.smem, stream, kv_map,
-                    p);
+  const dim3 grid(p.ctas * G.per_sm);
+  if (p.q8)
+    return launch_pdl(score_kernel<true>, grid, dim3(kThreads), G.smem, stream, kv_map, p);
+  return launch_pdl(score_kernel<false>, grid, dim3(kThreads), G.smem, stream, kv_map, p);
 }
 
 }  // namespace msa

@@ -44,6 +44,7 @@ class Workload:
     key_outlier_mult: float = 1.0
     topk_given: bool = False      # attend-only: draw the top-k list instead of scoring
     dense: bool = False           # dense decode: every visible block, no scoring or list
+    fp8_query: bool = False       # q quantised to fp8 e4m3 with a per-tensor scale
     pad_frac: float = 0.0         # fraction of requests with seq_len 0
     seq_args: dict = field(default_factory=dict)
 
@@ -56,7 +57,8 @@ class Workload:
                 "num_q_heads": self.num_q_heads, "num_kv_heads": self.num_kv_heads,
                 "head_dim": HEAD_DIM, "page": PAGE, "topk": TOPK, "seq_lens": self.seq_lens,
                 "pipeline": ("dense attend+combine" if self.dense else "attend+combine"
-                             if self.topk_given else "score+topk+attend+combine")}
+                             if self.topk_given else "score+topk+attend+combine"),
+                "query": "fp8 e4m3, per-tensor scale amax/448" if self.fp8_query else "bf16"}
 
 
 WORKLOADS = {
@@ -77,6 +79,10 @@ WORKLOADS = {
         # decode shapes
         Workload("dense_b16_q4_h64kv4_8k-32k", 16, 4, 64, 4, "uniform", seed=1006, kv_std=0.5,
                  kv_scale_mode="amax", dense=True, seq_args={"lo": 8192, "hi": 32768}),
+        # the batch-16 step with the query quantised to fp8 per tensor, the form
+        # the vLLM CUTLASS decode takes (query_fp8, q_scale)
+        Workload("b16_q4_h64kv4_8k-32k_fp8q", 16, 4, 64, 4, "uniform", seed=1007, kv_std=0.5,
+                 kv_scale_mode="amax", fp8_query=True, seq_args={"lo": 8192, "hi": 32768}),
     ]
 }
 
@@ -215,7 +221,7 @@ def all_visible_topk(seq_lens: list[int], qlen: int, hkv: int):
 @dataclass
 class StepInputs:
     """One layer's inputs, on `device`."""
-    q: torch.Tensor            # bf16 [T, Hq, 128]
+    q: torch.Tensor            # bf16 [T, Hq, 128], or fp8 e4m3 of value q * q_scale
     kv: torch.Tensor           # uint8 [NB, Hkv, 128, 256] (fp8 e4m3 bytes)
     block_table: torch.Tensor  # int32 [B, S]
     seq_lens: torch.Tensor     # int32 [B]
@@ -227,6 +233,7 @@ class StepInputs:
     num_q_heads: int
     num_kv_heads: int
     topk: torch.Tensor | None = None   # int32 [T, Hkv, 16] when given
+    q_scale: float = 1.0               # per-tensor scale of an fp8 q
 
     @property
     def batch(self) -> int:
@@ -269,11 +276,16 @@ def make_inputs(w: Workload | str, device="cpu", layer: int = 0,
     topk = None
     if w.topk_given:
         topk = draw_topk_given(seq_lens, w.qlen, w.num_kv_heads, gen_host).to(dev)
+    q_scale = 1.0
+    if w.fp8_query:   # per-tensor dynamic scale: the largest magnitude maps to 448
+        qf = q.float()
+        q_scale = float(qf.abs().max()) / FP8_MAX
+        q = (qf / q_scale).to(torch.float8_e4m3fn)
     return StepInputs(q=q, kv=kv, block_table=bt.to(dev),
                       seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=dev),
                       seq_lens_list=list(seq_lens), k_scale=k_scale, v_scale=v_scale,
                       sm_scale=HEAD_DIM ** -0.5, qlen=w.qlen, num_q_heads=w.num_q_heads,
-                      num_kv_heads=w.num_kv_heads, topk=topk)
+                      num_kv_heads=w.num_kv_heads, topk=topk, q_scale=q_scale)
 
 
 def make_custom(seq_lens: list[int], qlen: int, num_q_heads: int, num_kv_heads: int,

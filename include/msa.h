@@ -12,6 +12,7 @@
  *   msa_combine        merge of the split-K partials            (stage 4)
  *   msa_sparse_decode_select  stages 2 and 3 in one kernel
  *   msa_dense_decode   attention over every visible block (dense layers)
+ *   msa_*_q8           the same with an fp8 query and a per-tensor q_scale
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -223,6 +224,37 @@ int msa_dense_decode(const void *q, const void *kv, const int32_t *block_table,
                      const int32_t *seq_lens, void *workspace, size_t workspace_bytes, void *out,
                      int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
                      float k_scale, float v_scale, msa_stream_t stream);
+
+/*
+ * fp8 query variants.  The vLLM CUTLASS decode (msa_cutlass_sparse_decode on
+ * the vLLM pages) takes the query already quantised: query_fp8 with a
+ * per-tensor q_scale_float.  These entry points take that form: `q8` is fp8
+ * e4m3 (OCP "fn") [T, Hq, 128] whose value is q8 * q_scale, q_scale finite and
+ * > 0; every other argument, the operation, and the errors are those of the
+ * bf16 entry point of the same name.  The query tile is the fp8 rows as
+ * stored, so the scorer issues half the tensor-core work of the bf16 path
+ * (which carries each bf16 query exactly as two fp8 parts).
+ */
+int msa_score_q8(const void *q8, float q_scale, const void *kv, const int32_t *block_table,
+                 const int32_t *seq_lens, float *scores, int B, int Q, int Hq, int Hkv, int S,
+                 int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream);
+int msa_sparse_decode_q8(const void *q8, float q_scale, const void *kv,
+                         const int32_t *block_table, const int32_t *seq_lens, const int32_t *topk,
+                         void *workspace, size_t workspace_bytes, void *out, int B, int Q, int Hq,
+                         int Hkv, int S, int64_t num_blocks, float sm_scale, float k_scale,
+                         float v_scale, int num_splits, msa_stream_t stream);
+int msa_sparse_decode_select_q8(const void *q8, float q_scale, const void *kv,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                const float *scores, int64_t stride_h, int64_t stride_t,
+                                int64_t stride_n, int32_t *topk, void *workspace,
+                                size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv,
+                                int S, int64_t num_blocks, float sm_scale, float k_scale,
+                                float v_scale, int num_splits, msa_stream_t stream);
+int msa_dense_decode_q8(const void *q8, float q_scale, const void *kv,
+                        const int32_t *block_table, const int32_t *seq_lens, void *workspace,
+                        size_t workspace_bytes, void *out, int B, int Q, int Hq, int Hkv, int S,
+                        int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                        msa_stream_t stream);
 
 /*
  * msa_combine -- stage 4, merge of split-K partials ("fp32 split-K partials"

@@ -19,10 +19,16 @@ def q_bits(q: torch.Tensor) -> np.ndarray:
 
 
 def to_problem(inp, oracle):
-    return oracle.Problem(q_bits(inp.q), inp.kv.detach().cpu().numpy(),
+    """The oracle's problem for these inputs.  An fp8 query (value q * q_scale)
+    goes in as its codes decoded to bf16 (exact: every e4m3 value is a bf16
+    value) with sm_scale * q_scale."""
+    q, sm_scale = inp.q, inp.sm_scale
+    if q.dtype != torch.bfloat16:
+        q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
+    return oracle.Problem(q_bits(q), inp.kv.detach().cpu().numpy(),
                           inp.block_table.detach().cpu().numpy(),
                           inp.seq_lens.detach().cpu().numpy(), inp.qlen, inp.num_q_heads,
-                          inp.num_kv_heads, inp.sm_scale, inp.k_scale, inp.v_scale)
+                          inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
 
 
 def read_golden_rows(name: str) -> np.ndarray:

@@ -26,7 +26,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_and_binding_agree():
@@ -177,3 +177,14 @@ def test_dense_decode_rejects(lib):
     assert call(Q=33) == EINVAL
     assert call(vs=float("nan")) == EINVAL
     assert call(B=0) == 0                           # empty batch
+
+
+def test_fp8_query_entry_points_reject_bad_scales(lib):
+    for qs in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.msa_score_q8(A, qs, A, A, A, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0, None) == EINVAL
+        assert lib.msa_sparse_decode_q8(A, qs, A, A, A, A, None, 0, A, 16, 4, 64, 4, 8, 100, 0.088,
+                                        1.0, 1.0, 1, None) == EINVAL
+        assert lib.msa_dense_decode_q8(A, qs, A, A, A, A, 1 << 30, A, 16, 4, 64, 4, 8, 100, 0.088,
+                                       1.0, 1.0, None) == EINVAL
+    assert lib.msa_sparse_decode_select_q8(A, 1.0, A, A, A, None, 0, 0, 1, A, None, 0, A, 16, 4, 64,
+                                           4, 8, 100, 0.088, 1.0, 1.0, 1, None) == EINVAL

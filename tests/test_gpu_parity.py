@@ -11,7 +11,8 @@ import torch
 import block_sparse_gqa_score_gb300 as msa
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, to_problem)
+from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, q_bits,
+                           to_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -335,4 +336,46 @@ def test_dense_decode_graph_replay_after_lengths_change():
     ref = oracle.attend(to_problem(inp, oracle),
                         wl.all_visible_lists(lens_b, Q, Hkv, inp.stride).numpy())
     assert_out_close(_np(out), ref, padding_rows(lens_b, Q))
+    assert msa.get_error() == 0
+
+
+def _fp8_query(inp):
+    """The query quantised per tensor (scale = amax / 448, as vLLM's
+    scaled_fp8_quant with a dynamic scale), and the oracle problem for it: the
+    fp8 codes as bf16 (exact) with sm_scale * q_scale."""
+    qf = inp.q.float()
+    q_scale = float(qf.abs().max()) / 448.0
+    q8 = (qf / q_scale).to(torch.float8_e4m3fn)
+    p = oracle.Problem(q_bits(q8.to(torch.bfloat16)), inp.kv.cpu().numpy(),
+                       inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy(), inp.qlen,
+                       inp.num_q_heads, inp.num_kv_heads, inp.sm_scale * q_scale, inp.k_scale,
+                       inp.v_scale)
+    return q8, q_scale, p
+
+
+FP8Q_CASES = [([257, 513] * 2, 4, 64, 4), ([0, 2, 3, 130, 2048, 2049], 4, 16, 1),
+              ([2500, 700], 32, 16, 1), ([20000, 9000], 4, 64, 4)]
+
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", FP8Q_CASES)
+def test_fp8_query_matches_oracle(seq_lens, Q, Hq, Hkv):
+    """msa_*_q8: an fp8 query of value q8 * q_scale through the scorer, the
+    fused select-then-attend step, the attend on given lists and dense decode."""
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=113, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    q8, qs, p = _fp8_query(inp)
+    scores, tk, out = msa.decode_step(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                                      inp.k_scale, inp.v_scale, q_scale=qs)
+    s_gpu = _np(scores).astype(np.float64)
+    assert_scores_close(s_gpu, oracle.score(p))
+    assert np.array_equal(_np(tk), oracle.topk(s_gpu, np.array(seq_lens, dtype=np.int32), Q))
+    assert_out_close(_np(out), oracle.attend(p, _np(tk)), padding_rows(seq_lens, Q))
+    given = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(5))
+    out2 = msa.sparse_decode(q8, inp.kv, inp.block_table, inp.seq_lens, given.to(DEV), Q,
+                             inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=2, q_scale=qs)
+    assert_out_close(_np(out2), oracle.attend(p, given.numpy()), padding_rows(seq_lens, Q))
+    out3 = msa.dense_decode(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                            inp.k_scale, inp.v_scale, q_scale=qs)
+    lists = wl.all_visible_lists(seq_lens, Q, Hkv, inp.stride).numpy()
+    assert_out_close(_np(out3), oracle.attend(p, lists), padding_rows(seq_lens, Q))
     assert msa.get_error() == 0

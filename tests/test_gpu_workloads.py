@@ -46,14 +46,15 @@ def test_workload_full_size_sampled(name):
         # every visible block: the oracle attends over all-visible lists
         topk = wl.all_visible_lists(inp.seq_lens_list, inp.qlen, inp.num_kv_heads, inp.stride)
         out = msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
-                               inp.sm_scale, inp.k_scale, inp.v_scale)
+                               inp.sm_scale, inp.k_scale, inp.v_scale, q_scale=inp.q_scale)
     elif w.topk_given:
         topk = inp.topk
         out = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, inp.qlen,
-                                inp.sm_scale, inp.k_scale, inp.v_scale)
+                                inp.sm_scale, inp.k_scale, inp.v_scale, q_scale=inp.q_scale)
     else:
         scores, topk, out = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens,
-                                            inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale)
+                                            inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
+                                            q_scale=inp.q_scale)
         s_gpu = scores.cpu().numpy().astype(np.float64)
         # scores: sampled blocks against the oracle's definition
         triples = _sample_triples(inp, rng)
