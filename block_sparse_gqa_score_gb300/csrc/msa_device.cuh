@@ -303,6 +303,25 @@ __device__ __forceinline__ int store_query_e4m3(const uint4 (&raw)[8], int row0,
   return e;
 }
 
+// max(a, b, c) in one instruction (the three-input fp32 max of sm_100 and
+// later); exact, and like fmaxf it returns the other operands' max when one is
+// NaN.
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// The largest of 16 fp32 values held as raw bits (8 three-input maxima).
+__device__ __forceinline__ float max16(const uint32_t (&v)[16]) {
+  float a[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k)
+    a[k] = fmax3f(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                  __uint_as_float(v[3 * k + 2]));
+  return fmaxf(fmax3f(a[0], a[1], a[2]), fmax3f(a[3], a[4], __uint_as_float(v[15])));
+}
+
 // An fp8 e4m3 query token's 16 rows (16 heads x 128 B, contiguous) copied as
 // stored into rows row0 .. row0 + 15 of a 128B-swizzled K-major tile; lane l
 // moves 64 bytes of row l / 2.

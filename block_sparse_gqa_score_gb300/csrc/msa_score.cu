@@ -24,7 +24,9 @@
 //    the fp8 keys need no widening; it also writes the -inf tails;
 //  * warps 3-6 read the accumulator (one key per lane), take each token's max
 //    over its 16 heads and visible keys, and publish their four quarter-page
-//    maxima through shared memory and a per-slot mbarrier;
+//    maxima through shared memory and a per-slot mbarrier; with one CTA per
+//    SM (qlen >= 9, where this epilogue costs as much as the MMAs) warps 8-11
+//    take every other group of four tokens of the same lane quarters;
 //  * warp 7 combines the quarters and writes the scores.
 #include "msa_device.cuh"
 #include "msa_launch.h"
@@ -34,7 +36,8 @@ namespace msa {
 
 namespace {
 
-constexpr int kThreads = 256;       // 8 warps, see above
+// 8 warps, see above; 12 with a second set of epilogue warps (ScoreGeometry::threads)
+constexpr int kMaxWarps = 12;
 constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
 constexpr int kMaxStages = 8;
 constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
@@ -56,11 +59,13 @@ struct ScoreTail {
   uint32_t tmem_base;
   int start_b, start_rem, count;   // this CTA's page range
   int any_invalid;                 // some page of the range has a bad block-table entry
-  int64_t warp_sums[8];
+  int64_t warp_sums[kMaxWarps];
 };
 
 struct ScoreGeometry {
   int Q, nh, Qu, nacc, ncols, nqb, stages, per_sm;
+  int nsub;     // epilogue warps per TMEM lane quarter (2 with one CTA per SM)
+  int threads;  // 32 * (8 + 4 * (nsub - 1))
   int qtile_bytes;  // hi + lo query tiles of one unit: 2 x 16Q rows x 128 B
   int off_q, off_qmul, off_red, off_tail, smem;
 };
@@ -79,20 +84,25 @@ __host__ __device__ inline ScoreGeometry score_geometry(int Q) {
   G.ncols = nc;
   G.qtile_bytes = 2 * 16 * Q * 128;
   G.nqb = (2 * G.qtile_bytes <= 64 * 1024) ? 2 : 1;   // double-buffer small query tiles
-  const int fixed = G.nqb * G.qtile_bytes + align16(kQmulRing * Q * 4) +
-                    align16(kRedSlots * 4 * Q * 4) + align16(static_cast<int>(sizeof(ScoreTail))) +
-                    1024;
+  const int fixed1 = G.nqb * G.qtile_bytes + align16(kQmulRing * Q * 4) +
+                     align16(kRedSlots * 4 * Q * 4) + align16(static_cast<int>(sizeof(ScoreTail))) +
+                     1024;
   // two CTAs per SM (two independent pipelines) when tensor memory and shared
   // memory hold two; each then gets half an SM's shared memory
   const int two_budget = kSmemPerSM / 2 - 1024;
-  G.per_sm = (nc <= 256 && (two_budget - fixed) / kHalfTile >= 3) ? 2 : 1;
+  G.per_sm = (nc <= 256 && (two_budget - fixed1) / kHalfTile >= 3) ? 2 : 1;
+  // one CTA per SM has the registers for a second set of epilogue warps
+  G.nsub = G.per_sm == 1 ? 2 : 1;
+  G.threads = 32 * (8 + 4 * (G.nsub - 1));
+  const int red_bytes = align16(kRedSlots * 4 * G.nsub * Q * 4);
+  const int fixed = fixed1 - align16(kRedSlots * 4 * Q * 4) + red_bytes;
   const int budget = G.per_sm == 2 ? two_budget : kSmemLimit;
   int st = (budget - fixed) / kHalfTile;
   G.stages = st > kMaxStages ? kMaxStages : st;
   G.off_q = G.stages * kHalfTile;
   G.off_qmul = G.off_q + G.nqb * G.qtile_bytes;
   G.off_red = G.off_qmul + align16(kQmulRing * Q * 4);
-  G.off_tail = G.off_red + align16(kRedSlots * 4 * Q * 4);
+  G.off_tail = G.off_red + red_bytes;
   G.smem = G.off_tail + align16(static_cast<int>(sizeof(ScoreTail))) + 1024;
   return G;
 }
@@ -188,10 +198,13 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
 // At most 128 registers: registers are allocated per SM sub-partition (16K
 // each), so two 7-warp CTAs per SM need <= 128 per thread.  kFp8Q: the query
 // is fp8 (q8 * q_scale), compiled separately so that the bf16 kernel carries
-// none of its branches.
-template <bool kFp8Q>
+// none of its branches.  kWide: the second set of epilogue warps (one CTA
+// per SM), likewise a separate instantiation.
+template <bool kFp8Q, bool kWide>
 __global__ void __maxnreg__(128)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
+  constexpr int kSub = kWide ? 2 : 1;              // epilogue warps per TMEM lane quarter
+  constexpr int kNumThreads = 32 * (8 + 4 * (kSub - 1));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -200,7 +213,7 @@ __global__ void __maxnreg__(128)
   uint8_t* stages = smem;                                              // [stages][128][128 B]
   uint8_t* qtiles = smem + G.off_q;                                    // [nqb][hi, lo][16Q][128 B]
   float* qmul_ring = reinterpret_cast<float*>(smem + G.off_qmul);      // [kQmulRing][Q]
-  float* red = reinterpret_cast<float*>(smem + G.off_red);             // [kRedSlots][4][Q]
+  float* red = reinterpret_cast<float*>(smem + G.off_red);             // [kRedSlots][4][nsub][Q]
   ScoreTail* tail = reinterpret_cast<ScoreTail*>(smem + G.off_tail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int T = p.B * Q;
@@ -208,7 +221,7 @@ __global__ void __maxnreg__(128)
 
   // ---- this CTA's page range: block-wide prefix sum over the requests -----------
   {
-    const int per = (p.B + kThreads - 1) / kThreads;
+    const int per = (p.B + kNumThreads - 1) / kNumThreads;
     const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
     int64_t local = 0;
     for (int b = b_lo; b < b_hi; ++b) {
@@ -226,7 +239,7 @@ __global__ void __maxnreg__(128)
     if (lane == 31) tail->warp_sums[warp] = incl;
     __syncthreads();
     int64_t before = 0, total = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < kNumThreads / 32; ++w) {
       if (w < warp) before += tail->warp_sums[w];
       total += tail->warp_sums[w];
     }
@@ -253,18 +266,18 @@ __global__ void __maxnreg__(128)
     }
     for (int s = 0; s < kMaxAcc; ++s) {
       mbar_init(&tail->dfull[s], 1);
-      mbar_init(&tail->dempty[s], 4);
+      mbar_init(&tail->dempty[s], 4 * kSub);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tail->qfull[s], 1);
       mbar_init(&tail->qempty[s], 1);
     }
     for (int s = 0; s < kRedSlots; ++s) {
-      mbar_init(&tail->red_full[s], 4);
+      mbar_init(&tail->red_full[s], 4 * kSub);
       mbar_init(&tail->red_empty[s], 1);
     }
     for (int s = 0; s < kQmulRing; ++s) mbar_init(&tail->qmul_ready[s], 1);
-    mbar_init(&tail->finish, 8);
+    mbar_init(&tail->finish, kNumThreads / 32);
     tail->any_invalid = 0;
     fence_barrier_init();
   } else if (warp == 1) {
@@ -283,7 +296,7 @@ __global__ void __maxnreg__(128)
   // roles need no per-page table reads on their critical path.
   bool all_valid = true;
   if (warp != 0 && warp != 2) {
-    const int nthr = kThreads - 64, t_id = tid - (warp == 1 ? 32 : 64);
+    const int nthr = kNumThreads - 64, t_id = tid - (warp == 1 ? 32 : 64);
     const int t0 = static_cast<int>(static_cast<int64_t>(count) * t_id / nthr);
     const int t1 = static_cast<int>(static_cast<int64_t>(count) * (t_id + 1) / nthr);
     if (t0 < t1) {
@@ -297,7 +310,7 @@ __global__ void __maxnreg__(128)
       }
       if (bad) atomicOr(&tail->any_invalid, 1);
     }
-    named_barrier(2, kThreads - 64);   // no wait precedes it: warps 1, 3-7 all arrive
+    named_barrier(2, kNumThreads - 64);  // no wait precedes it: warps 1 and 3+ all arrive
     all_valid = *reinterpret_cast<volatile int*>(&tail->any_invalid) == 0;
   }
 
@@ -448,6 +461,7 @@ __global__ void __maxnreg__(128)
   } else if (warp != 7) {
     // ---- epilogue: accumulator -> per-token block maxima ----------------------------
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
+    const int sub = (kWide && warp >= 8) ? 1 : 0;  // which epilogue set (groups of 4 tokens)
     const int key = 32 * quarter + lane;         // key (row of the page) of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     PageWalk w;
@@ -470,7 +484,7 @@ __global__ void __maxnreg__(128)
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
         // groups of four tokens: four TMEM loads in flight under one wait, then
         // four independent tree maxima and four back-to-back warp reductions
-        for (int j0 = 0; j0 < ntok; j0 += 4) {
+        for (int j0 = 4 * sub; j0 < ntok; j0 += 4 * kSub) {
           const int nj = min(4, ntok - j0);
           if (lim_base + tok0 + j0 + nj - 1 < 0) continue;   // warp-uniform: nothing visible
           uint32_t v[4][16];
@@ -481,12 +495,7 @@ __global__ void __maxnreg__(128)
           int ord[4];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
-            float m8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              m8[e] = fmaxf(__uint_as_float(v[jj][e]), __uint_as_float(v[jj][e + 8]));
-            const float m = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float m = max16(v[jj]);
             const int lim = lim_base + tok0 + j0 + jj;
             ord[jj] = order_int((jj < nj && key <= lim) ? m : -INFINITY);
           }
@@ -507,7 +516,8 @@ __global__ void __maxnreg__(128)
         if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
         break;
       }
-      if (lane < Q) red[(slot * 4 + quarter) * Q + lane] = myv;
+      // this set's row of the quarter (-inf for the tokens the other set takes)
+      if (lane < Q) red[((slot * 4 + quarter) * kSub + sub) * Q + lane] = myv;
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->red_full[slot]);
       ++vp;
@@ -551,7 +561,7 @@ __global__ void __maxnreg__(128)
       if (lane < Q) {
         float v = -INFINITY;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) v = fmaxf(v, red[(slot * 4 + q4) * Q + lane]);
+        for (int r = 0; r < 4 * kSub; ++r) v = fmaxf(v, red[(slot * 4 * kSub + r) * Q + lane]);
         p.scores[row0 + static_cast<int64_t>(lane) * p.S] = (v == -INFINITY) ? v : v * qm;
       }
       __syncwarp();
@@ -571,7 +581,8 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    for (auto* k : {score_kernel<false>, score_kernel<true>}) {
+    for (auto* k : {score_kernel<false, false>, score_kernel<true, false>,
+                    score_kernel<false, true>, score_kernel<true, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemLimit);
       if (r != cudaSuccess) return r;
@@ -584,10 +595,12 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.ctas * G.per_sm);
-  if (p.q8)
-    return launch_pdl(score_kernel<true>, grid, dim3(kThreads), G.smem, stream, kv_map, p);
-  return launch_pdl(score_kernel<false>, grid, dim3(kThreads), G.smem, stream, kv_map, p);
+  const dim3 grid(p.ctas * G.per_sm), block(G.threads);
+  if (G.nsub == 2)
+    return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, kv_map, p)
+                : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, kv_map, p);
+  return p.q8 ? launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, kv_map, p)
+              : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, kv_map, p);
 }
 
 }  // namespace msa
