@@ -38,6 +38,7 @@ namespace {
 
 // 8 warps, see above; 12 with a second set of epilogue warps (ScoreGeometry::threads)
 constexpr int kMaxWarps = 12;
+constexpr int kWideSub = 2;      // epilogue warp sets when one CTA runs per SM
 constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
 constexpr int kMaxStages = 8;
 constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
@@ -92,7 +93,7 @@ __host__ __device__ inline ScoreGeometry score_geometry(int Q) {
   const int two_budget = kSmemPerSM / 2 - 1024;
   G.per_sm = (nc <= 256 && (two_budget - fixed1) / kHalfTile >= 3) ? 2 : 1;
   // one CTA per SM has the registers for a second set of epilogue warps
-  G.nsub = G.per_sm == 1 ? 2 : 1;
+  G.nsub = G.per_sm == 1 ? kWideSub : 1;
   G.threads = 32 * (8 + 4 * (G.nsub - 1));
   const int red_bytes = align16(kRedSlots * 4 * G.nsub * Q * 4);
   const int fixed = fixed1 - align16(kRedSlots * 4 * Q * 4) + red_bytes;
@@ -203,7 +204,7 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
 template <bool kFp8Q, bool kWide>
 __global__ void __maxnreg__(128)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
-  constexpr int kSub = kWide ? 2 : 1;              // epilogue warps per TMEM lane quarter
+  constexpr int kSub = kWide ? kWideSub : 1;              // epilogue warps per TMEM lane quarter
   constexpr int kNumThreads = 32 * (8 + 4 * (kSub - 1));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -596,7 +597,7 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   });
   if (e != cudaSuccess) return e;
   const dim3 grid(p.ctas * G.per_sm), block(G.threads);
-  if (G.nsub == 2)
+  if (G.nsub > 1)   // the wide instantiation (kWide) is the one built for G.threads
     return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, kv_map, p)
                 : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, kv_map, p);
   return p.q8 ? launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, kv_map, p)
