@@ -25,8 +25,9 @@
 //  * warps 3-6 read the accumulator (one key per lane), take each token's max
 //    over its 16 heads and visible keys, and publish their four quarter-page
 //    maxima through shared memory and a per-slot mbarrier; with one CTA per
-//    SM (qlen >= 9, where this epilogue costs as much as the MMAs) warps 8-11
-//    take every other group of four tokens of the same lane quarters;
+//    SM (qlen >= 8, where this epilogue costs as much as the MMAs) warps 8-15
+//    form two more sets on the same lane quarters, the three sets taking
+//    groups of two tokens in turn;
 //  * warp 7 combines the quarters and writes the scores.
 #include "msa_device.cuh"
 #include "msa_launch.h"
@@ -36,9 +37,9 @@ namespace msa {
 
 namespace {
 
-// 8 warps, see above; 12 with a second set of epilogue warps (ScoreGeometry::threads)
-constexpr int kMaxWarps = 12;
-constexpr int kWideSub = 2;      // epilogue warp sets when one CTA runs per SM
+// 8 warps, see above; 16 with the extra epilogue warp sets (ScoreGeometry::threads)
+constexpr int kMaxWarps = 16;
+constexpr int kWideSub = 3;      // epilogue warp sets when one CTA runs per SM
 constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
 constexpr int kMaxStages = 8;
 constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
@@ -205,6 +206,7 @@ template <bool kFp8Q, bool kWide>
 __global__ void __maxnreg__(128)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
   constexpr int kSub = kWide ? kWideSub : 1;              // epilogue warps per TMEM lane quarter
+  constexpr int kGrp = kWide ? 2 : 4;              // tokens per epilogue group
   constexpr int kNumThreads = 32 * (8 + 4 * (kSub - 1));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -462,7 +464,7 @@ __global__ void __maxnreg__(128)
   } else if (warp != 7) {
     // ---- epilogue: accumulator -> per-token block maxima ----------------------------
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
-    const int sub = (kWide && warp >= 8) ? 1 : 0;  // which epilogue set (groups of 4 tokens)
+    const int sub = kWide ? (warp >= 12 ? 2 : (warp >= 8 ? 1 : 0)) : 0;  // epilogue set
     const int key = 32 * quarter + lane;         // key (row of the page) of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     PageWalk w;
@@ -485,25 +487,25 @@ __global__ void __maxnreg__(128)
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
         // groups of four tokens: four TMEM loads in flight under one wait, then
         // four independent tree maxima and four back-to-back warp reductions
-        for (int j0 = 4 * sub; j0 < ntok; j0 += 4 * kSub) {
-          const int nj = min(4, ntok - j0);
+        for (int j0 = kGrp * sub; j0 < ntok; j0 += kGrp * kSub) {
+          const int nj = min(kGrp, ntok - j0);
           if (lim_base + tok0 + j0 + nj - 1 < 0) continue;   // warp-uniform: nothing visible
-          uint32_t v[4][16];
+          uint32_t v[kGrp][16];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
+          for (int jj = 0; jj < kGrp; ++jj)
             if (jj < nj) tc::ld_32x32b_x16(lane_addr + buf * 16 * G.Qu + (j0 + jj) * 16, v[jj]);
           tc::wait_ld();
-          int ord[4];
+          int ord[kGrp];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
+          for (int jj = 0; jj < kGrp; ++jj) {
             const float m = max16(v[jj]);
             const int lim = lim_base + tok0 + j0 + jj;
             ord[jj] = order_int((jj < nj && key <= lim) ? m : -INFINITY);
           }
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) ord[jj] = __reduce_max_sync(0xffffffffu, ord[jj]);
+          for (int jj = 0; jj < kGrp; ++jj) ord[jj] = __reduce_max_sync(0xffffffffu, ord[jj]);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
+          for (int jj = 0; jj < kGrp; ++jj)
             if (jj < nj && lane == tok0 + j0 + jj) myv = order_float(ord[jj]);
         }
         tc::fence_before_thread_sync();
