@@ -25,9 +25,9 @@
 //  * warps 3-6 read the accumulator (one key per lane), take each token's max
 //    over its 16 heads and visible keys, and publish their four quarter-page
 //    maxima through shared memory and a per-slot mbarrier; with one CTA per
-//    SM (qlen >= 8, where this epilogue costs as much as the MMAs) warps 8-15
-//    form two more sets on the same lane quarters, the three sets taking
-//    groups of two tokens in turn;
+//    SM (qlen >= 8, where this epilogue costs as much as the MMAs) warps 8-19
+//    form three more sets on the same lane quarters, the four sets taking
+//    groups of two tokens in turn (20 warps: registers capped near 96);
 //  * warp 7 combines the quarters and writes the scores.
 #include "msa_device.cuh"
 #include "msa_launch.h"
@@ -37,9 +37,9 @@ namespace msa {
 
 namespace {
 
-// 8 warps, see above; 16 with the extra epilogue warp sets (ScoreGeometry::threads)
-constexpr int kMaxWarps = 16;
-constexpr int kWideSub = 3;      // epilogue warp sets when one CTA runs per SM
+// 8 warps, see above; 20 with the extra epilogue warp sets (ScoreGeometry::threads)
+constexpr int kMaxWarps = 20;
+constexpr int kWideSub = 4;      // epilogue warp sets when one CTA runs per SM
 constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
 constexpr int kMaxStages = 8;
 constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
@@ -200,10 +200,11 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
 // At most 128 registers: registers are allocated per SM sub-partition (16K
 // each), so two 7-warp CTAs per SM need <= 128 per thread.  kFp8Q: the query
 // is fp8 (q8 * q_scale), compiled separately so that the bf16 kernel carries
-// none of its branches.  kWide: the second set of epilogue warps (one CTA
-// per SM), likewise a separate instantiation.
+// none of its branches.  kWide: the extra sets of epilogue warps (one CTA
+// per SM, 640 threads), likewise a separate instantiation; the launch bounds
+// keep 128 registers for the two-CTA kernel.
 template <bool kFp8Q, bool kWide>
-__global__ void __maxnreg__(128)
+__global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
   constexpr int kSub = kWide ? kWideSub : 1;              // epilogue warps per TMEM lane quarter
   constexpr int kGrp = kWide ? 2 : 4;              // tokens per epilogue group
@@ -464,7 +465,7 @@ __global__ void __maxnreg__(128)
   } else if (warp != 7) {
     // ---- epilogue: accumulator -> per-token block maxima ----------------------------
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
-    const int sub = kWide ? (warp >= 12 ? 2 : (warp >= 8 ? 1 : 0)) : 0;  // epilogue set
+    const int sub = kWide ? (warp >= 8 ? (warp - 4) / 4 : 0) : 0;  // epilogue set
     const int key = 32 * quarter + lane;         // key (row of the page) of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     PageWalk w;
