@@ -32,6 +32,13 @@
 //        the running sums.  When a page's O^T is ready the same
 //        thread owns one value dim d (one TMEM lane of O^T) and accumulates
 //        O = O * alpha + O_page in registers, so O is never rescaled in place.
+// The CTA's page list is the top-k list (given, or selected in the prologue
+// from the block scores: select mode), or in dense decode (the TensorRT-LLM PR
+// dense-decode commit: the first layers attend the whole page table) a range
+// of consecutive visible blocks.  An fp8 query (value q8 * q_scale, as
+// msa_cutlass_sparse_decode takes it) goes into the hi part as stored, with a
+// zero lo part.  Dense decode and the fp8 query are template flags, so the
+// bf16 list-mode kernel carries none of their branches.
 #include "msa_device.cuh"
 #include "msa_launch.h"
 #include "msa_select.cuh"

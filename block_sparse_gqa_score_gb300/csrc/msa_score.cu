@@ -16,12 +16,14 @@
 //  * warp 1 issues, from one thread, kind::f8f6f4 MMAs with the fp8 K tile
 //    straight from the TMA stage as operand A (M = 128 keys, K-major) and the
 //    request's Q x 16 query rows as operand B (N = 16 Q), accumulating fp32 in
-//    double-buffered tensor memory;
+//    two or four tensor-memory accumulator buffers;
 //  * warp 2 prepares the query tile of each (request, KV head) unit of the
 //    range: the bf16 query, scaled per token by a power of two 2^-e, is
 //    represented exactly as the sum of two fp8 e4m3 parts (bf16's 8
 //    significant bits are 4 + 4) that accumulate into the same columns, so
-//    the fp8 keys need no widening; it also writes the -inf tails;
+//    the fp8 keys need no widening (an fp8 query, value q8 * q_scale, is the
+//    hi part as stored and only its MMAs are issued: half the tensor work);
+//    it also writes the -inf tails;
 //  * warps 3-6 read the accumulator (one key per lane), take each token's max
 //    over its 16 heads and visible keys, and publish their four quarter-page
 //    maxima through shared memory and a per-slot mbarrier; with one CTA per

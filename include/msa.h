@@ -96,9 +96,10 @@ typedef struct CUstream_st *msa_stream_t;
  * where K8 is the fp8 key as stored (the cache's K half).  Blocks n > cur(i)
  * and every block of a padding row get -inf.  The whole [Hkv, T, S] buffer is
  * written.  sm_scale > 0 and k_scale > 0 (both finite) are required.
- * Numerics: fp8 keys are widened exactly; each query row is scaled by a power
- * of two and rounded to fp16 (exact for the row's elements down to 2^-28 of
- * its largest one), products accumulate in fp32.
+ * Numerics: the fp8 key tile is a tensor-core operand as stored; each (token,
+ * KV head)'s query rows are scaled by a power of two (largest magnitude in
+ * [2^7, 2^8)) and carried as the sum of two fp8 e4m3 parts, which is exact for
+ * every element down to 2^-9 of the largest; products accumulate in fp32.
  * Errors: MSA_EINVAL for Q outside 1..32, Hq != 16*Hkv, S < 1, num_blocks < 1,
  * num_blocks*Hkv*128 >= 2^31, null or non-16-byte-aligned q/kv, null
  * block_table/seq_lens/scores.  Device: MSA_ERR_PAGE_RANGE (block scored
