@@ -273,11 +273,11 @@ int msa_combine(const void *workspace, void *out, int T, int Hq, int num_splits,
 
 /*
  * msa_sparse_decode_static -- msa_sparse_decode for callers that cannot
- * allocate device memory.  The paper has no counterpart for it; it exists for
- * callers that only hold the step's inputs and outputs: a plugin or operator
- * interface that gives the library no workspace, or a runtime that forbids
- * cudaMalloc on its hot path (an allocation can block on the whole device or
- * fail under memory pressure).
+ * allocate device memory.  The vLLM and TensorRT-LLM pages have no counterpart
+ * for it; it exists for callers that only hold the step's inputs and outputs:
+ * a plugin or operator interface that gives the library no workspace, or a
+ * runtime that forbids cudaMalloc on its hot path (an allocation can block on
+ * the whole device or fail under memory pressure).
  *
  * Same arguments and result as msa_sparse_decode without the workspace pair.
  * The split-K partials go to one scratch array compiled into the library:
