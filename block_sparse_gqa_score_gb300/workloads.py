@@ -75,6 +75,11 @@ WORKLOADS = {
         Workload("b16_q32_h64kv4_256k_outliers", 16, 32, 64, 4, "fixed", seed=1005,
                  key_outlier_frac=0.05, key_outlier_mult=8.0,
                  seq_args={"values": [262144] * 16}),
+        # the qlen-32 workload on 2 requests: the same kernels at a size a
+        # full profiler capture can take (about 1 GB on the device)
+        Workload("b2_q32_h64kv4_256k_outliers", 2, 32, 64, 4, "fixed", seed=1008,
+                 key_outlier_frac=0.05, key_outlier_mult=8.0,
+                 seq_args={"values": [262144] * 2}),
         # the same model's dense layers (every visible block) on the batch-16
         # decode shapes
         Workload("dense_b16_q4_h64kv4_8k-32k", 16, 4, 64, 4, "uniform", seed=1006, kv_std=0.5,
