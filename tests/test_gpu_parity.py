@@ -379,3 +379,43 @@ def test_fp8_query_matches_oracle(seq_lens, Q, Hq, Hkv):
     lists = wl.all_visible_lists(seq_lens, Q, Hkv, inp.stride).numpy()
     assert_out_close(_np(out3), oracle.attend(p, lists), padding_rows(seq_lens, Q))
     assert msa.get_error() == 0
+
+
+def test_dense_decode_skips_and_flags_a_bad_page():
+    """A block-table entry out of range in dense decode: that block is skipped
+    and MSA_ERR_PAGE_RANGE set; the rest equals the oracle over every other
+    visible block (the current block's and an earlier block's entries)."""
+    seq_lens, Q, Hq, Hkv = [9000, 3000], 2, 32, 2
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=114, device=DEV, kv_std=0.5)
+    for b, n in [(0, 20), (1, (seq_lens[1] - 1) // 128)]:   # an earlier block; a current one
+        bt = inp.block_table.clone()
+        bt[b, n] = inp.num_blocks + 3
+        out = msa.dense_decode(inp.q, inp.kv, bt, inp.seq_lens, Q, inp.sm_scale, inp.k_scale,
+                               inp.v_scale)
+        assert msa.get_error() & msa._native.ERR_PAGE_RANGE
+        lists = wl.all_visible_lists(seq_lens, Q, Hkv, inp.stride)
+        sub = lists[b * Q:(b + 1) * Q]                # a view: the skipped block goes
+        sub[sub == n] = -1
+        assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), lists.numpy()),
+                         padding_rows(seq_lens, Q))
+
+
+def test_fp8_query_select_attend_with_splits():
+    """The fused select-then-attend step with an fp8 query and two splits
+    equals the separate selector and attend on the same query."""
+    seq_lens, Q, Hq, Hkv = [20000, 9000, 300], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=115, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    q8, qs, p = _fp8_query(inp)
+    scores = msa.score(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale,
+                       q_scale=qs)
+    tk, out = msa.sparse_decode_select(q8, inp.kv, inp.block_table, inp.seq_lens, scores, Q,
+                                       inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=2,
+                                       q_scale=qs)
+    tk2 = msa.topk(scores, inp.seq_lens, Q)
+    assert torch.equal(tk, tk2)
+    sep = msa.sparse_decode(q8, inp.kv, inp.block_table, inp.seq_lens, tk2, Q, inp.sm_scale,
+                            inp.k_scale, inp.v_scale, num_splits=2, q_scale=qs)
+    assert torch.equal(out, sep)
+    assert_out_close(_np(out), oracle.attend(p, _np(tk)), padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
