@@ -227,14 +227,18 @@ def _traffic_from_profiles(stage: str, workload: str):
 
 def _work(inp, topk_cpu: np.ndarray | None, reads_lists: bool = True):
     """Algorithmic bytes per launch of each stage, and the scorer's useful flops."""
-    B, Q, Hq, Hkv, S = inp.batch, inp.qlen, inp.num_q_heads, inp.num_kv_heads, inp.stride
-    T = B * Q
+    B, Hq, Hkv, S = inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.stride
+    # query tokens per request (one length per request in a prefill batch)
+    q_lens = inp.q_lens if inp.q_lens is not None else [inp.qlen] * B
+    first = np.concatenate([[0], np.cumsum(q_lens)]).astype(int)
+    T = int(first[-1])
     pages = [math.ceil(L / 128) for L in inp.seq_lens_list]
     q_bytes = T * Hq * 128 * inp.q.element_size()   # bf16, or an fp8 query
     out_bytes = T * Hq * 128 * 2
     score = sum(pages) * Hkv * 16384 + q_bytes + Hkv * T * S * 4 + B * S * 4
     cand = 0
     for b, L in enumerate(inp.seq_lens_list):
+        Q = q_lens[b]
         for j in range(Q):
             pos = L - Q + j
             if pos >= 0:
@@ -243,11 +247,11 @@ def _work(inp, topk_cpu: np.ndarray | None, reads_lists: bool = True):
     topk = cand * Hkv * 4 + T * Hkv * 16 * 4
     # the scorer's products: every visible page-head's 128 keys against its
     # group's 16 heads x Q tokens, 128-dim dot products
-    score_flops = sum(pages) * Hkv * 2.0 * 128 * 128 * 16 * Q
+    score_flops = sum(n * Q for n, Q in zip(pages, q_lens)) * Hkv * 2.0 * 128 * 128 * 16
     union = per_token = 0
     if topk_cpu is not None:
         for b in range(B):
-            rows = topk_cpu[b * Q:(b + 1) * Q]          # [Q, Hkv, 16]
+            rows = topk_cpu[first[b]:first[b + 1]]      # [q_len, Hkv, 16]
             for g in range(Hkv):
                 ids = rows[:, g, :]
                 ids = ids[ids >= 0]
@@ -278,14 +282,15 @@ def run_reference(args, rank, world):
     def step(k):
         b, g = units[k % len(units)]
         _oracle_unit(p, inp, oracle, b, g, cores, given)
+        return _unit_tokens(inp, b)
 
     for k in range(args.warmup):
         step(k)
     t0 = time.perf_counter()
+    tokens = 0.0
     for k in range(args.steps):
-        step(args.warmup + k)
+        tokens += step(args.warmup + k)
     dt = time.perf_counter() - t0
-    tokens = args.steps * inp.qlen / inp.num_kv_heads
     v = tokens / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
@@ -299,7 +304,7 @@ def run_reference(args, rank, world):
                                           "visible block" if w.dense else
                                           "scores of all its visible blocks, selection of its "
                                           "query rows, attention of its query rows x 16 heads")
-                                       + "; counted as qlen/Hkv query tokens"},
+                                       + "; counted as its query tokens / Hkv"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -316,20 +321,40 @@ def _given_lists(w, inp):
     return None
 
 
-def _problem(inp, oracle):
+def _problem(inp, oracle, b=None):
+    """The oracle's problem: the whole batch, or (a prefill batch) request b
+    alone with Q = its query length, so that its tokens sit at the last
+    positions of its sequence."""
     # an fp8 query (value q * q_scale): its codes as bf16 (exact) with sm_scale * q_scale
     q, sm_scale = inp.q, inp.sm_scale
     if q.dtype != torch.bfloat16:
         q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
-    return oracle.Problem(q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16),
-                          inp.kv.cpu().numpy(), inp.block_table.cpu().numpy(),
-                          inp.seq_lens.cpu().numpy(), inp.qlen, inp.num_q_heads,
+    bits = q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    bt, sl, Q = inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy(), inp.qlen
+    if inp.q_lens is not None:
+        if b is None:
+            return None   # built per request by _oracle_unit
+        s0, Q = sum(inp.q_lens[:b]), inp.q_lens[b]
+        bits, bt, sl = bits[s0:s0 + Q], bt[b:b + 1], sl[b:b + 1]
+    return oracle.Problem(bits, inp.kv.cpu().numpy(), bt, sl, Q, inp.num_q_heads,
                           inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
+
+
+def _unit_tokens(inp, b) -> float:
+    """Query tokens one (request, KV head) unit stands for: its request's / Hkv."""
+    Q = inp.q_lens[b] if inp.q_lens is not None else inp.qlen
+    return Q / inp.num_kv_heads
 
 
 def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
     """The oracle's whole pipeline for one (request, KV head) unit."""
     Q, G = inp.qlen, inp.num_q_heads // inp.num_kv_heads
+    if inp.q_lens is not None:
+        # a prefill request: its own problem, its rows of the given lists
+        s0, Q = sum(inp.q_lens[:b]), inp.q_lens[b]
+        rows = [j * inp.num_q_heads + g * G + h for j in range(Q) for h in range(G)]
+        oracle.attend_rows(_problem(inp, oracle, b), topk_given[s0:s0 + Q], rows, nthreads)
+        return
     L = inp.seq_lens_list[b]
     cur = (L - 1) // 128
     if topk_given is None:
@@ -353,16 +378,17 @@ def cpu_baseline(inp, w, lists, budget_s: float = 12.0):
     cores = oracle.default_threads()
     units = [(b, g) for b in range(inp.batch) for g in range(inp.num_kv_heads)
              if inp.seq_lens_list[b] > 0]
-    done = 0
+    done, tokens = 0, 0.0
     t0 = time.perf_counter()
     for b, g in units:
         _oracle_unit(p, inp, oracle, b, g, cores, lists)
         done += 1
+        tokens += _unit_tokens(inp, b)
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    tokens = done * inp.qlen / inp.num_kv_heads
-    what = ("attend only, given top-k" if w.topk_given else "dense attend, every visible block"
+    what = ("prefill attend, given per-token top-k" if w.prefill_q else
+            "attend only, given top-k" if w.topk_given else "dense attend, every visible block"
             if w.dense else "score, select, attend")
     sample = (f"{done} of {len(units)} (request, KV head) units of layer 0, each the whole "
               f"oracle pipeline ({what})")
@@ -391,15 +417,25 @@ def run_ours(args, rank, world, local):
     layer_bytes = first.kv.numel() + first.q.numel() * 2
     n_layers = max(2, math.ceil(4 * l2 / max(layer_bytes, 1)))
     layers = [first] + [wl.make_inputs(w, device=dev, layer=l) for l in range(1, n_layers)]
-    splits = msa.choose_splits(w.batch, w.qlen, w.num_kv_heads, props.multi_processor_count)
+    T = first.tokens   # every layer has the same request and query lengths
+    # buffers and splits sized by tokens: B requests of qlen, or T prefill tokens
+    tb, tq = (1, T) if w.prefill_q else (w.batch, w.qlen)
+    splits = msa.choose_splits(tb, tq, w.num_kv_heads, props.multi_processor_count)
     if w.dense:   # the split count of dense decode follows the block table's stride
         splits = max(msa.dense_splits(inp.stride) for inp in layers)
-    bufs = [msa.DecodeBuffers.allocate(w.batch, w.qlen, w.num_q_heads, w.num_kv_heads,
-                                       inp.stride, dev, splits) for inp in layers]
+    bufs = [msa.DecodeBuffers.allocate(tb, tq, w.num_q_heads, w.num_kv_heads, inp.stride, dev,
+                                       splits) for inp in layers]
     stream = torch.cuda.Stream(dev)
 
     def stage_calls(l):
         inp, bf = layers[l], bufs[l]
+        if w.prefill_q:
+            return [lambda: None, lambda: None,
+                    lambda: msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                               inp.cu_seqlens_q, inp.topk, inp.sm_scale,
+                                               inp.k_scale, inp.v_scale, out=bf.out,
+                                               num_splits=bf.num_splits, workspace=bf.workspace,
+                                               q_scale=inp.q_scale)]
         if w.dense:
             return [lambda: None, lambda: None,
                     lambda: msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens,
@@ -561,7 +597,6 @@ def run_ours(args, rank, world, local):
         b.synchronize()
         attend_alone_ms = _max_over_ranks(a.elapsed_time(b), world) / reps_stage
     flags |= msa.get_error(clear=True)
-    T = w.tokens
     value = world * T * args.steps / (total_ms / 1e3)
     peak, peak_kind = _peaks()
     mean_work = {k: sum(x[k] for x in works) / len(works) for k in works[0]}
@@ -601,11 +636,16 @@ def run_ours(args, rank, world, local):
                     "note": f"of {peak_kind}; " + note.format("bytes")}
     gathered = {"GB/s": mean_work["attend_kv_bytes"] / (attend_alone_ms / 1e3) / 1e9,
                 "kernel": ("attend_kernel over every visible block (msa_dense_decode)"
-                           if w.dense else "attend_kernel on the step's lists (msa_sparse_decode)"),
+                           if w.dense else "attend_kernel on each token's list "
+                           "(msa_sparse_prefill)" if w.prefill_q else
+                           "attend_kernel on the step's lists (msa_sparse_decode)"),
                 "ms": attend_alone_ms,
                 "union_pages_per_step": mean_work["union_pages"],
                 "token_pages_per_step": mean_work["token_pages"]}
     gathered["frac_of_hbm"] = gathered["GB/s"] / peak
+    # what the kernel's CTAs load (each token's own pages; pages shared by a
+    # request's tokens come again, mostly from L2) per second
+    gathered["token_pages_GB/s"] = mean_work["token_pages"] * 32768 / (attend_alone_ms / 1e3) / 1e9
     if fused:
         gathered["fused_select_attend_frac_of_hbm"] = (
             mean_work["attend_kv_bytes"] / (avg_ms["attend"] / 1e3) / 1e9 / peak)
@@ -639,6 +679,8 @@ def _to_cpu(inp):
     c.q, c.kv, c.block_table, c.seq_lens = (inp.q.cpu(), inp.kv.cpu(), inp.block_table.cpu(),
                                             inp.seq_lens.cpu())
     c.topk = inp.topk.cpu() if inp.topk is not None else None
+    if inp.cu_seqlens_q is not None:
+        c.cu_seqlens_q = inp.cu_seqlens_q.cpu()
     return c
 
 
@@ -657,6 +699,8 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
 
     def layout(inp):
         parts = [("q", inp.q), ("seq_lens", inp.seq_lens), ("block_table", inp.block_table)]
+        if w.prefill_q:
+            parts.append(("cu_seqlens_q", inp.cu_seqlens_q))
         if w.topk_given:
             parts.append(("topk", inp.topk))
         offs, off = {}, 0
@@ -691,7 +735,12 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
     def compute(k):
         l = k % n_layers
         inp, bf, v = layers[l], bufs[l], views[l]
-        if w.topk_given:
+        if w.prefill_q:
+            msa.sparse_prefill(v["q"], inp.kv, v["block_table"], v["seq_lens"], v["cu_seqlens_q"],
+                               v["topk"], inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
+                               num_splits=bf.num_splits, workspace=bf.workspace,
+                               q_scale=inp.q_scale)
+        elif w.topk_given:
             msa.sparse_decode(v["q"], inp.kv, v["block_table"], v["seq_lens"], v["topk"],
                               inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale, out=bf.out,
                               num_splits=bf.num_splits, workspace=bf.workspace,
@@ -768,7 +817,7 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
         b.record()
         torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b)
-    return {"value": world * w.tokens * steps / (ms / 1e3), "unit": UNIT,
+    return {"value": world * layers[0].tokens * steps / (ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
             "ms_per_step": ms / steps, "path": mode}
 

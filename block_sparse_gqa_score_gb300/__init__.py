@@ -6,6 +6,8 @@ vLLM MiniMax-M3 sparse attention pages and TensorRT-LLM PR #17171 describe it:
   score()          per-block causal max of scaled q.k over each KV head's group
   topk()           top-16 blocks (current block kept, ties to the lower index)
   sparse_decode()  split-K attention over the selected pages (+ merge)
+  sparse_prefill() the same attend for prefill batches (one query length per
+                   request, cu_seqlens_q)
   combine()        merge of split-K partials
   decode_step()    the three stages back to back on one stream
 
@@ -35,7 +37,8 @@ TOPK = 16
 GROUP = 16
 MAX_QLEN = 32
 
-__all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "dense_decode", "dense_splits",
+__all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "sparse_prefill",
+           "sparse_prefill_select", "dense_decode", "dense_splits",
            "combine", "decode_step",
            "fused_selection", "FUSED_MAX_BLOCKS", "workspace_bytes",
            "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
@@ -69,7 +72,8 @@ _KV_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 _FP8_Q = getattr(torch, "float8_e4m3fn", None)
 
 
-def _geometry(q, kv, block_table, seq_lens, qlen):
+def _geometry(q, kv, block_table, seq_lens, qlen: int | None):
+    """Shapes of a step's inputs; q must hold B * qlen tokens (qlen None: any)."""
     _need(q, "q", (torch.bfloat16,) + ((_FP8_Q,) if _FP8_Q is not None else ()))
     dev = q.device
     _need(kv, "kv", _KV_DTYPES, dev)
@@ -84,7 +88,7 @@ def _geometry(q, kv, block_table, seq_lens, qlen):
     B, S = block_table.shape
     Hkv = kv.shape[1]
     Hq = q.shape[1]
-    if q.shape[0] != B * qlen:
+    if qlen is not None and q.shape[0] != B * qlen:
         raise ValueError(f"q has {q.shape[0]} tokens, expected B*qlen = {B * qlen}")
     return dev, int(B), int(S), int(Hq), int(Hkv), int(kv.shape[0])
 
@@ -264,6 +268,88 @@ def sparse_decode_select(q, kv, block_table, seq_lens, scores, qlen: int, sm_sca
     else:
         status = _lib().msa_sparse_decode_select(q.data_ptr(), *args)
     _native.check(status, "msa_sparse_decode_select")
+    return topk_out, out
+
+
+def _prefill_geometry(q, kv, block_table, seq_lens, cu_seqlens_q):
+    """Shapes of a prefill-style batch: q holds T tokens, request b owning
+    tokens cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, None)
+    _need(cu_seqlens_q, "cu_seqlens_q", (torch.int32,), dev)
+    if tuple(cu_seqlens_q.shape) != (B + 1,):
+        raise ValueError("cu_seqlens_q must be [B + 1]")
+    return dev, B, int(q.shape[0]), S, Hq, Hkv, NB
+
+
+def _prefill_splits(T: int, Hq: int, Hkv: int, num_splits: int, workspace, dev):
+    splits = num_splits if num_splits > 0 else choose_splits(1, max(T, 1), Hkv)
+    need = workspace_bytes(1, max(T, 1), Hq, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return splits, ws_ptr, ws_bytes
+
+
+def sparse_prefill(q, kv, block_table, seq_lens, cu_seqlens_q, topk_idx, sm_scale: float,
+                   k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
+                   num_splits: int = 0, workspace: torch.Tensor | None = None, stream=None,
+                   q_scale: float = 1.0) -> torch.Tensor:
+    """Sparse attend of a prefill or chunked-prefill batch (msa_sparse_prefill):
+    request b's query tokens are q[cu_seqlens_q[b] : cu_seqlens_q[b + 1]], the
+    last ones of its seq_lens[b]; each token attends its own list
+    topk_idx [T, Hkv, 16].  Returns bf16 [T, Hq, 128]."""
+    dev, B, T, S, Hq, Hkv, NB = _prefill_geometry(q, kv, block_table, seq_lens, cu_seqlens_q)
+    _need(topk_idx, "topk", (torch.int32,), dev)
+    if tuple(topk_idx.shape) != (T, Hkv, TOPK):
+        raise ValueError("topk must be [T, Hkv, 16]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    splits, ws_ptr, ws_bytes = _prefill_splits(T, Hq, Hkv, num_splits, workspace, dev)
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), cu_seqlens_q.data_ptr(),
+            topk_idx.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(), B, T, Hq, Hkv, S, NB,
+            float(sm_scale), float(k_scale), float(v_scale), splits, _stream(dev, stream))
+    if _fp8(q, q_scale):
+        st = _lib().msa_sparse_prefill_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        st = _lib().msa_sparse_prefill(q.data_ptr(), *args)
+    _native.check(st, "msa_sparse_prefill")
+    return out
+
+
+def sparse_prefill_select(q, kv, block_table, seq_lens, cu_seqlens_q, scores, sm_scale: float,
+                          k_scale: float = 1.0, v_scale: float = 1.0,
+                          topk_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                          num_splits: int = 0, workspace: torch.Tensor | None = None,
+                          stream=None, q_scale: float = 1.0):
+    """Per-token causal top-16 selected from `scores` [Hkv, T, >= S] (any
+    strides) and attended, for a prefill-style batch
+    (msa_sparse_prefill_select).  Returns (topk [T, Hkv, 16], out)."""
+    dev, B, T, S, Hq, Hkv, NB = _prefill_geometry(q, kv, block_table, seq_lens, cu_seqlens_q)
+    if not (isinstance(scores, torch.Tensor) and scores.is_cuda and scores.dtype == torch.float32
+            and scores.device == dev):
+        raise TypeError("scores must be a float32 tensor on q's device")
+    if scores.dim() != 3 or scores.shape[0] != Hkv or scores.shape[1] != T \
+            or scores.shape[2] < S:
+        raise ValueError("scores must be [Hkv, T, >= S]")
+    if topk_out is None:
+        topk_out = torch.empty((T, Hkv, TOPK), dtype=torch.int32, device=dev)
+    _need(topk_out, "topk_out", (torch.int32,), dev)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    splits, ws_ptr, ws_bytes = _prefill_splits(T, Hq, Hkv, num_splits, workspace, dev)
+    sh, st, sn = scores.stride()
+    args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), cu_seqlens_q.data_ptr(),
+            scores.data_ptr(), sh, st, sn, topk_out.data_ptr(), ws_ptr, ws_bytes, out.data_ptr(),
+            B, T, Hq, Hkv, S, NB, float(sm_scale), float(k_scale), float(v_scale), splits,
+            _stream(dev, stream))
+    if _fp8(q, q_scale):
+        status = _lib().msa_sparse_prefill_select_q8(q.data_ptr(), float(q_scale), *args)
+    else:
+        status = _lib().msa_sparse_prefill_select(q.data_ptr(), *args)
+    _native.check(status, "msa_sparse_prefill_select")
     return topk_out, out
 
 

@@ -22,7 +22,8 @@ EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode", "msa_combine", "msa_get_error", "msa_strerror", "msa_version",
            "msa_sparse_decode_static", "msa_sparse_decode_select", "msa_dense_splits",
            "msa_dense_decode", "msa_score_q8", "msa_sparse_decode_q8",
-           "msa_sparse_decode_select_q8", "msa_dense_decode_q8")
+           "msa_sparse_decode_select_q8", "msa_dense_decode_q8", "msa_sparse_prefill",
+           "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8")
 
 _lib = None
 _lock = threading.Lock()
@@ -73,6 +74,15 @@ def load(path: str | None = None):
         lib.msa_sparse_decode_select_q8.argtypes = ([P, f32] +
                                                     lib.msa_sparse_decode_select.argtypes[1:])
         lib.msa_dense_decode_q8.argtypes = [P, f32] + lib.msa_dense_decode.argtypes[1:]
+        # prefill: cu_seqlens_q after seq_lens, (B, T) in place of (B, Q)
+        lib.msa_sparse_prefill.argtypes = [P, P, P, P, P, P, P, sz, P, i32, i32, i32, i32, i32,
+                                           i64, f32, f32, f32, i32, P]
+        lib.msa_sparse_prefill_select.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, sz, P,
+                                                  i32, i32, i32, i32, i32, i64, f32, f32, f32,
+                                                  i32, P]
+        lib.msa_sparse_prefill_q8.argtypes = [P, f32] + lib.msa_sparse_prefill.argtypes[1:]
+        lib.msa_sparse_prefill_select_q8.argtypes = ([P, f32] +
+                                                     lib.msa_sparse_prefill_select.argtypes[1:])
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
@@ -80,7 +90,8 @@ def load(path: str | None = None):
                      "msa_combine", "msa_get_error", "msa_version", "msa_sparse_decode_static",
                      "msa_sparse_decode_select", "msa_dense_splits", "msa_dense_decode",
                      "msa_score_q8", "msa_sparse_decode_q8", "msa_sparse_decode_select_q8",
-                     "msa_dense_decode_q8"):
+                     "msa_dense_decode_q8", "msa_sparse_prefill", "msa_sparse_prefill_select",
+                     "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -251,14 +251,23 @@ void dense_split(int S, int* nsplit, int* span) {
 // null means `topk` is the input list; otherwise the lists are selected from
 // the strided scores inside the attend kernel and written to `topk`.
 // dense_span > 0: no list, every visible block (msa_dense_decode).
+// cu_q non-null: a prefill-style batch of T tokens, request b owning tokens
+// [cu_q[b], cu_q[b + 1]) (msa_sparse_prefill); Q is then unused.
 int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
                   const int32_t* seq_lens, const float* scores, int64_t stride_h,
                   int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
                   size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
                   int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
-                  int num_splits, msa_stream_t stream, int dense_span = 0, float q_scale = 0.f) {
+                  int num_splits, msa_stream_t stream, int dense_span = 0, float q_scale = 0.f,
+                  const int32_t* cu_q = nullptr, int T = 0) {
   if (!(q_scale == 0.f || finite_pos(q_scale))) return MSA_EINVAL;
-  int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
+  if (cu_q) {
+    // the token count takes the place of B * Q in every size below
+    if (dense_span != 0 || !aligned(cu_q, 4) || T < 0 || T > INT_MAX / 4 || (B == 0) != (T == 0))
+      return MSA_EINVAL;
+    if (T == 0) return B == 0 ? MSA_OK : MSA_EINVAL;
+  }
+  int st = check_common(q, kv, block_table, seq_lens, B, cu_q ? 1 : Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
   if (dense_span == 0 && (!topk || !aligned(topk, 4))) return MSA_EINVAL;
   if (!out || !aligned(out, 16) || !finite_pos(sm_scale) ||
@@ -270,13 +279,15 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   if (B == 0) return MSA_OK;
   DeviceState* dev;
   if ((st = device_state(&dev)) != MSA_OK) return st;
-  const int splits = num_splits == 0 ? msa_choose_splits(B, Q, Hkv, dev->sm_count) : num_splits;
-  const size_t need = msa_workspace_bytes(B, Q, Hq, splits);
+  // sizes over tokens: B requests of Q, or T tokens of a prefill-style batch
+  const int tb = cu_q ? 1 : B, tq = cu_q ? T : Q;
+  const int splits = num_splits == 0 ? msa_choose_splits(tb, tq, Hkv, dev->sm_count) : num_splits;
+  const size_t need = msa_workspace_bytes(tb, tq, Hq, splits);
   if (splits > 1 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
     return MSA_ENOSPC;
   CUtensorMap map;
   if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
-  const int64_t rows = static_cast<int64_t>(B) * Q * Hq;
+  const int64_t rows = static_cast<int64_t>(tb) * tq * Hq;
   msa::AttendParams p{};
   p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
   p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
@@ -303,6 +314,8 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   p.num_blocks = num_blocks;
   p.logit_scale = sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
+  p.cu_q = cu_q;
+  p.T = cu_q ? T : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = from_cuda(msa::launch_attend(map, p, s))) != MSA_OK) return st;
   if (splits > 1)
@@ -393,6 +406,59 @@ int msa_dense_decode_q8(const void* q8, float q_scale, const void* kv,
   return sparse_decode(q8, kv, block_table, seq_lens, nullptr, 0, 0, 0, nullptr, workspace,
                        workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale, k_scale,
                        v_scale, nsplit, stream, span, q_scale);
+}
+
+// Prefill and chunked prefill: B requests, request b's query tokens being
+// [cu_seqlens_q[b], cu_seqlens_q[b + 1]) of the T tokens, at the last positions
+// of its seq_lens[b].  Same lists, numerics and errors as msa_sparse_decode.
+int msa_sparse_prefill(const void* q, const void* kv, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                       const int32_t* topk, void* workspace, size_t workspace_bytes, void* out,
+                       int B, int T, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                       float k_scale, float v_scale, int num_splits, msa_stream_t stream) {
+  if (!cu_seqlens_q) return MSA_EINVAL;
+  return sparse_decode(q, kv, block_table, seq_lens, nullptr, 0, 0, 0, const_cast<int32_t*>(topk),
+                       workspace, workspace_bytes, out, B, 1, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, 0.f, cu_seqlens_q, T);
+}
+
+int msa_sparse_prefill_q8(const void* q8, float q_scale, const void* kv,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          const int32_t* cu_seqlens_q, const int32_t* topk, void* workspace,
+                          size_t workspace_bytes, void* out, int B, int T, int Hq, int Hkv, int S,
+                          int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                          int num_splits, msa_stream_t stream) {
+  if (!cu_seqlens_q || !finite_pos(q_scale)) return MSA_EINVAL;
+  return sparse_decode(q8, kv, block_table, seq_lens, nullptr, 0, 0, 0, const_cast<int32_t*>(topk),
+                       workspace, workspace_bytes, out, B, 1, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, q_scale, cu_seqlens_q, T);
+}
+
+int msa_sparse_prefill_select(const void* q, const void* kv, const int32_t* block_table,
+                              const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                              const float* scores, int64_t stride_h, int64_t stride_t,
+                              int64_t stride_n, int32_t* topk, void* workspace,
+                              size_t workspace_bytes, void* out, int B, int T, int Hq, int Hkv,
+                              int S, int64_t num_blocks, float sm_scale, float k_scale,
+                              float v_scale, int num_splits, msa_stream_t stream) {
+  if (!cu_seqlens_q || !scores) return MSA_EINVAL;
+  return sparse_decode(q, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
+                       workspace, workspace_bytes, out, B, 1, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, 0.f, cu_seqlens_q, T);
+}
+
+int msa_sparse_prefill_select_q8(const void* q8, float q_scale, const void* kv,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* cu_seqlens_q, const float* scores,
+                                 int64_t stride_h, int64_t stride_t, int64_t stride_n,
+                                 int32_t* topk, void* workspace, size_t workspace_bytes,
+                                 void* out, int B, int T, int Hq, int Hkv, int S,
+                                 int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                                 int num_splits, msa_stream_t stream) {
+  if (!cu_seqlens_q || !scores || !finite_pos(q_scale)) return MSA_EINVAL;
+  return sparse_decode(q8, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
+                       workspace, workspace_bytes, out, B, 1, Hq, Hkv, S, num_blocks, sm_scale,
+                       k_scale, v_scale, num_splits, stream, 0, q_scale, cu_seqlens_q, T);
 }
 
 int msa_get_error(unsigned int* flags, int clear) {

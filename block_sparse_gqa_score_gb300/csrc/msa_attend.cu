@@ -107,10 +107,43 @@ __device__ __forceinline__ void fill(float (&a)[N], float v) {
   for (int k = 0; k < N; ++k) a[k] = v;
 }
 
+// Request of query token i in a variable-length batch whose request r owns
+// tokens [cu_q[r], cu_q[r + 1]): b is the number of requests that end at or
+// before i, found by a 32-way search across the warp (each round probes 32
+// evenly spaced request ends and keeps the sub-range where the prefix of ends
+// <= i stops).  Every probe reads cu_q[1..B].  Returns false, with b = 0, when
+// token i lies in no request's range (cu_q not ascending, or i outside
+// [cu_q[0], cu_q[B])); otherwise b, the token's offset j and the request's
+// query length.  Warp-uniform arguments; all 32 lanes call it.
+__device__ __forceinline__ bool varlen_token(const int32_t* __restrict__ cu_q, int B, int i,
+                                             int lane, int& b, int& j, int& qlen) {
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int step = (hi - lo + 31) >> 5;
+    const int r = lo + (lane + 1) * step - 1;
+    const bool before = r < hi && cu_q[r + 1] <= i;
+    const int k = __popc(__ballot_sync(0xffffffffu, before));
+    lo += k * step;
+    hi = min(hi, lo + step - 1);
+  }
+  b = 0;
+  j = 0;
+  qlen = 1;
+  if (lo >= B) return false;
+  const int start = cu_q[lo], end = cu_q[lo + 1];
+  if (i < start || i >= end) return false;
+  b = lo;
+  j = i - start;
+  qlen = end - start;
+  return true;
+}
+
 // kDense: dense decode (every visible block of the CTA's range, no list);
-// kFp8Q: an fp8 query (q8 * q_scale).  Each is compiled separately so that the
-// bf16 list-mode kernel carries none of their branches.
-template <bool kDense, bool kFp8Q>
+// kFp8Q: an fp8 query (q8 * q_scale); kVarlen: prefill-style batches, one
+// query length per request (cu_q), grid.x = T tokens.  Each is compiled
+// separately so that the bf16 list-mode decode kernel carries none of their
+// branches.
+template <bool kDense, bool kFp8Q, bool kVarlen = false>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap kv_map, const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -127,10 +160,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int g = blockIdx.y;      // KV head
   const int split = blockIdx.z;  // split-K part
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = i / p.Q, j = i - b * p.Q;
 
   // ---- prologue ------------------------------------------------------------------
   if (warp == 0) {
+    // the token's request b, its offset j there and the request's query length
+    int b, j, qlen;
+    bool tok_ok = true;
+    if constexpr (kVarlen) {
+      tok_ok = varlen_token(p.cu_q, p.B, i, lane, b, j, qlen);
+    } else {
+      b = i / p.Q;
+      j = i - b * p.Q;
+      qlen = p.Q;
+    }
     // this CTA's page list, barriers, and the first loads.  The request's
     // block-table row goes into stage 2 while seq_lens is read: every lane
     // has all its loads in flight at once, so the row costs one round trip.
@@ -147,9 +189,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (32 * k + lane < ncopy) table_s[32 * k + lane] = v[k];
     }
     __syncwarp();
-    const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
+    // a prefill request's tokens are the last qlen of its sequence: the
+    // context before them (L - qlen) cannot be negative
+    const bool seq_ok = tok_ok && L >= 0 && (L == 0 || (L - 1) / kPage < p.S) &&
+                        (!kVarlen || L >= qlen);
     if (!seq_ok && lane == 0) flag_error(p.err, MSA_ERR_SEQ_RANGE);
-    const int pos = seq_ok ? L - p.Q + j : -1;
+    const int pos = seq_ok ? L - qlen + j : -1;
     const int64_t list = (static_cast<int64_t>(i) * p.Hkv + g) * kTopK;
     // The current block comes first in a CTA's page order when it is listed
     // (split 0 then owns it), and it always is in select mode and in the
@@ -606,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           p.out[(row0 + h) * kHeadDim + d] = static_cast<uint16_t>(f32_to_bf16_bits(o[h] * f));
         }
       } else {
-        const int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hq;
+        const int64_t rows = static_cast<int64_t>(kVarlen ? p.T : p.B * p.Q) * p.Hq;
         const int64_t base = static_cast<int64_t>(split) * rows + row0;
 #pragma unroll
         for (int h = 0; h < kGroup; ++h) p.part_o[(base + h) * kHeadDim + d] = o[h] * p.v_scale;
@@ -674,7 +719,8 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
     for (auto* k : {attend_kernel<false, false>, attend_kernel<true, false>,
-                    attend_kernel<false, true>, attend_kernel<true, true>}) {
+                    attend_kernel<false, true>, attend_kernel<true, true>,
+                    attend_kernel<false, false, true>, attend_kernel<false, true, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (r != cudaSuccess) return r;
@@ -686,9 +732,14 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  const int T = p.B * p.Q;
+  const int T = p.cu_q ? p.T : p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
   const dim3 block(kThreads);
+  if (p.cu_q)  // prefill-style batches take lists only (no dense mode)
+    return p.q8 ? launch_pdl(attend_kernel<false, true, true>, grid, block, kSmemBytes, stream,
+                             kv_map, p)
+                : launch_pdl(attend_kernel<false, false, true>, grid, block, kSmemBytes, stream,
+                             kv_map, p);
   if (p.q8)
     return p.dense_span > 0
                ? launch_pdl(attend_kernel<true, true>, grid, block, kSmemBytes, stream, kv_map, p)

@@ -58,6 +58,10 @@ struct AttendParams {
   float v_scale;
   const uint8_t* q8;           // fp8 e4m3 [T, Hq, 128], value q8 * q_scale; or nullptr
   float q_scale;
+  // prefill-style batches: request r owns tokens [cu_q[r], cu_q[r + 1]) of the
+  // T tokens (then Q is unused); nullptr: every request has Q tokens
+  const int32_t* cu_q;
+  int T;
 };
 
 // Runs `set_up` once per device (e.g. raising a kernel's dynamic shared-memory

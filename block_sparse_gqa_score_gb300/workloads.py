@@ -47,18 +47,29 @@ class Workload:
     fp8_query: bool = False       # q quantised to fp8 e4m3 with a per-tensor scale
     pad_frac: float = 0.0         # fraction of requests with seq_len 0
     seq_args: dict = field(default_factory=dict)
+    # chunked prefill: request b's query is its last q_len_b tokens, q_len_b
+    # drawn uniformly in [lo, hi] (at most seq_len), each token with its own
+    # drawn top-k list (then qlen is unused)
+    prefill_q: tuple | None = None
 
     @property
     def tokens(self) -> int:
+        if self.prefill_q is not None:
+            raise ValueError("a prefill workload's token count depends on its draws")
         return self.batch * self.qlen
 
     def describe(self) -> dict:
-        return {"workload": self.name, "batch": self.batch, "decode_query_len": self.qlen,
-                "num_q_heads": self.num_q_heads, "num_kv_heads": self.num_kv_heads,
-                "head_dim": HEAD_DIM, "page": PAGE, "topk": TOPK, "seq_lens": self.seq_lens,
-                "pipeline": ("dense attend+combine" if self.dense else "attend+combine"
-                             if self.topk_given else "score+topk+attend+combine"),
-                "query": "fp8 e4m3, per-tensor scale amax/448" if self.fp8_query else "bf16"}
+        d = {"workload": self.name, "batch": self.batch, "decode_query_len": self.qlen,
+             "num_q_heads": self.num_q_heads, "num_kv_heads": self.num_kv_heads,
+             "head_dim": HEAD_DIM, "page": PAGE, "topk": TOPK, "seq_lens": self.seq_lens,
+             "pipeline": ("dense attend+combine" if self.dense else "attend+combine"
+                          if self.topk_given else "score+topk+attend+combine"),
+             "query": "fp8 e4m3, per-tensor scale amax/448" if self.fp8_query else "bf16"}
+        if self.prefill_q is not None:
+            del d["decode_query_len"]
+            d["prefill_query_lens"] = f"uniform {self.prefill_q[0]}-{self.prefill_q[1]}"
+            d["pipeline"] = "prefill attend (msa_sparse_prefill), given per-token top-k"
+        return d
 
 
 WORKLOADS = {
@@ -88,6 +99,11 @@ WORKLOADS = {
         # the vLLM CUTLASS decode takes (query_fp8, q_scale)
         Workload("b16_q4_h64kv4_8k-32k_fp8q", 16, 4, 64, 4, "uniform", seed=1007, kv_std=0.5,
                  kv_scale_mode="amax", fp8_query=True, seq_args={"lo": 8192, "hi": 32768}),
+        # chunked prefill on the same model: 4 requests of 8k-32k tokens, each
+        # with a 1k-2k query chunk at its end, every token with its own list
+        Workload("prefill_b4_chunk1k-2k_h64kv4_8k-32k", 4, 0, 64, 4, "uniform", seed=1009,
+                 kv_std=0.5, kv_scale_mode="amax", topk_given=True, prefill_q=(1024, 2048),
+                 seq_args={"lo": 8192, "hi": 32768}),
     ]
 }
 
@@ -167,43 +183,55 @@ def draw_kv(nb: int, hkv: int, gen: torch.Generator, device, std: float = 1.0,
     return kv, k_scale, v_scale
 
 
-def draw_topk_given(seq_lens: list[int], qlen: int, hkv: int, gen: torch.Generator):
+def draw_topk_varlen(q_lens: list[int], seq_lens: list[int], hkv: int, gen: torch.Generator):
     """Attend-only input: per (token, KV head), the token's current block plus
     up to 15 distinct blocks drawn uniformly from the earlier ones, ascending,
-    -1 padded.  Padding rows (no visible token) are all -1."""
-    B = len(seq_lens)
-    out = torch.full((B * qlen, hkv, TOPK), -1, dtype=torch.int32)
-    for b, L in enumerate(seq_lens):
+    -1 padded.  Request b's q_lens[b] tokens are the last ones of its
+    seq_lens[b], rows request-major; rows with no visible token are all -1."""
+    out = torch.full((sum(q_lens), hkv, TOPK), -1, dtype=torch.int32)
+    i = 0
+    for L, qlen in zip(seq_lens, q_lens):
         for j in range(qlen):
             visible = L - qlen + j + 1          # tokens this query row may see
-            if visible <= 0:
-                continue
-            cur = (visible - 1) // PAGE
-            for g in range(hkv):
-                if cur + 1 <= TOPK:
-                    ids = list(range(cur + 1))
-                else:
-                    pick = torch.randperm(cur, generator=gen)[:TOPK - 1]
-                    ids = sorted(pick.tolist()) + [cur]
-                out[b * qlen + j, g, :len(ids)] = torch.tensor(ids, dtype=torch.int32)
+            if visible > 0:
+                cur = (visible - 1) // PAGE
+                for g in range(hkv):
+                    if cur + 1 <= TOPK:
+                        ids = list(range(cur + 1))
+                    else:
+                        pick = torch.randperm(cur, generator=gen)[:TOPK - 1]
+                        ids = sorted(pick.tolist()) + [cur]
+                    out[i, g, :len(ids)] = torch.tensor(ids, dtype=torch.int32)
+            i += 1
+    return out
+
+
+def draw_topk_given(seq_lens: list[int], qlen: int, hkv: int, gen: torch.Generator):
+    """draw_topk_varlen with qlen tokens for every request."""
+    return draw_topk_varlen([qlen] * len(seq_lens), seq_lens, hkv, gen)
+
+
+def all_visible_lists_varlen(q_lens: list[int], seq_lens: list[int], hkv: int, width: int):
+    """Every visible page ascending, -1 padded to `width` columns, for request
+    b's q_lens[b] last tokens: the lists that make the sparse attend dense (the
+    vLLM prefill test's lists while a row sees at most 16 pages)."""
+    out = torch.full((sum(q_lens), hkv, width), -1, dtype=torch.int32)
+    i = 0
+    for L, qlen in zip(seq_lens, q_lens):
+        for j in range(qlen):
+            visible = L - qlen + j + 1
+            if visible > 0:
+                n = math.ceil(visible / PAGE)
+                if n > width:
+                    raise ValueError("more visible pages than columns")
+                out[i, :, :n] = torch.arange(n, dtype=torch.int32)
+            i += 1
     return out
 
 
 def all_visible_lists(seq_lens: list[int], qlen: int, hkv: int, width: int):
-    """Every visible page ascending, -1 padded to `width` columns: the lists
-    that make the sparse attend dense (any number of pages)."""
-    B = len(seq_lens)
-    out = torch.full((B * qlen, hkv, width), -1, dtype=torch.int32)
-    for b, L in enumerate(seq_lens):
-        for j in range(qlen):
-            visible = L - qlen + j + 1
-            if visible <= 0:
-                continue
-            n = math.ceil(visible / PAGE)
-            if n > width:
-                raise ValueError("more visible pages than columns")
-            out[b * qlen + j, :, :n] = torch.arange(n, dtype=torch.int32)
-    return out
+    """all_visible_lists_varlen with qlen tokens for every request."""
+    return all_visible_lists_varlen([qlen] * len(seq_lens), seq_lens, hkv, width)
 
 
 def all_visible_topk(seq_lens: list[int], qlen: int, hkv: int):
@@ -239,6 +267,11 @@ class StepInputs:
     num_kv_heads: int
     topk: torch.Tensor | None = None   # int32 [T, Hkv, 16] when given
     q_scale: float = 1.0               # per-tensor scale of an fp8 q
+    # a prefill batch: request b's q_lens[b] query tokens are the last ones of
+    # its seq_lens[b] (context seq_lens[b] - q_lens[b] tokens already cached),
+    # rows cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1; qlen is then 0
+    q_lens: list | None = None
+    cu_seqlens_q: torch.Tensor | None = None   # int32 [B + 1]
 
     @property
     def batch(self) -> int:
@@ -246,7 +279,7 @@ class StepInputs:
 
     @property
     def tokens(self) -> int:
-        return self.batch * self.qlen
+        return sum(self.q_lens) if self.q_lens is not None else self.batch * self.qlen
 
     @property
     def num_blocks(self) -> int:
@@ -269,6 +302,17 @@ def make_inputs(w: Workload | str, device="cpu", layer: int = 0,
     gen_host = torch.Generator().manual_seed(w.seed)
     if seq_lens is None:
         seq_lens = _draw_seq_lens(w, gen_host)
+    if w.prefill_q is not None:
+        lo, hi = w.prefill_q
+        q_lens = torch.randint(lo, hi + 1, (len(seq_lens),), generator=gen_host).tolist()
+        q_lens = [min(n, L) for n, L in zip(q_lens, seq_lens)]
+        inp = make_prefill(q_lens, seq_lens, w.num_q_heads, w.num_kv_heads,
+                           seed=w.seed * 1000 + layer, device=device, kv_std=w.kv_std,
+                           kv_scale_mode=w.kv_scale_mode, fp8_query=w.fp8_query)
+        inp.topk = draw_topk_varlen(q_lens, seq_lens, w.num_kv_heads,
+                                    torch.Generator().manual_seed(w.seed * 1000 + layer + 5)
+                                    ).to(inp.q.device)
+        return inp
     gen_host = torch.Generator().manual_seed(w.seed * 1000 + layer)
     bt, nb = paged_layout(seq_lens, gen_host)
     dev = torch.device(device)
@@ -314,3 +358,37 @@ def make_custom(seq_lens: list[int], qlen: int, num_q_heads: int, num_kv_heads: 
                       seq_lens_list=list(seq_lens), k_scale=k_scale, v_scale=v_scale,
                       sm_scale=HEAD_DIM ** -0.5, qlen=qlen, num_q_heads=num_q_heads,
                       num_kv_heads=num_kv_heads)
+
+
+def make_prefill(q_lens: list[int], seq_lens: list[int], num_q_heads: int, num_kv_heads: int,
+                 seed: int, device="cpu", kv_std: float = 1.0, kv_scale_mode: str = "unit",
+                 min_stride: int = 1, fp8_query: bool = False) -> StepInputs:
+    """Seeded inputs of a prefill or chunked-prefill batch (the vLLM prefill
+    test's recipe: q ~ N(0, 1) in bf16, K and V as draw_kv, pages scattered by
+    paged_layout): request b's q_lens[b] query tokens are the last ones of its
+    seq_lens[b], as MiniMaxM3SparsePrefillMetadata describes them.  With
+    fp8_query the query is quantised per tensor (scale amax / 448)."""
+    if len(q_lens) != len(seq_lens) or any(q < 0 or q > L for q, L in zip(q_lens, seq_lens)):
+        raise ValueError("need one q_len per request with 0 <= q_len <= seq_len")
+    gen_host = torch.Generator().manual_seed(seed)
+    bt, nb = paged_layout(seq_lens, gen_host, min_stride=min_stride)
+    dev = torch.device(device)
+    gen_dev = torch.Generator(device=dev).manual_seed(seed + 17)
+    kv, k_scale, v_scale = draw_kv(nb, num_kv_heads, gen_dev, dev, std=kv_std,
+                                   scale_mode=kv_scale_mode)
+    q = torch.randn((sum(q_lens), num_q_heads, HEAD_DIM), generator=gen_dev, device=dev,
+                    dtype=torch.bfloat16)
+    q_scale = 1.0
+    if fp8_query:
+        qf = q.float()
+        q_scale = float(qf.abs().max()) / FP8_MAX
+        q = (qf / q_scale).to(torch.float8_e4m3fn)
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + n)
+    return StepInputs(q=q, kv=kv, block_table=bt.to(dev),
+                      seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=dev),
+                      seq_lens_list=list(seq_lens), k_scale=k_scale, v_scale=v_scale,
+                      sm_scale=HEAD_DIM ** -0.5, qlen=0, num_q_heads=num_q_heads,
+                      num_kv_heads=num_kv_heads, q_scale=q_scale, q_lens=list(q_lens),
+                      cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=dev))

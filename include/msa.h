@@ -258,6 +258,75 @@ int msa_dense_decode_q8(const void *q8, float q_scale, const void *kv,
                         msa_stream_t stream);
 
 /*
+ * msa_sparse_prefill -- the sparse attend for prefill and chunked prefill:
+ * minimax_m3_sparse_attn on the vLLM pages (MiniMaxM3SparseTritonImpl.forward,
+ * the prefill part [nd:] of the batch, with MiniMaxM3SparsePrefillMetadata).
+ * B requests with one query length each: request b owns query tokens
+ * cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1 of the T tokens of q, and they
+ * are the last q_len_b = cu_seqlens_q[b + 1] - cu_seqlens_q[b] tokens of its
+ * sequence: token j of request b sits at position
+ *
+ *   pos = context_len_b + j,  context_len_b = seq_lens[b] - q_len_b,
+ *
+ * (the vLLM prefill test's visible-page count (seq_len - q_len + local_q) /
+ * 128 + 1).  Each token attends the blocks of its own list topk[i, g, :]
+ * [T, Hkv, 16] with the causal bound 128*n + t <= pos; the operation, output
+ * layout [T, Hq, 128], numerics and device errors are msa_sparse_decode's,
+ * which this call equals when every request has the same query length.
+ * cu_seqlens_q: int32 [B + 1] on the device, cu_seqlens_q[0] = 0, ascending,
+ * cu_seqlens_q[B] = T (read by the kernel only, so it may be written by an
+ * earlier kernel on `stream`).  Workspace for num_splits > 1:
+ * msa_workspace_bytes(1, T, Hq, splits); num_splits = 0 chooses
+ * msa_choose_splits(1, T, Hkv, sm_count).
+ * Errors: as msa_sparse_decode, plus null or misaligned cu_seqlens_q, T < 0
+ * or T > INT_MAX / 4, or exactly one of B and T zero (MSA_EINVAL); no query
+ * length bound applies.  Device: a token in no request's range (e.g. past
+ * cu_seqlens_q[B] < T) or of a request with q_len_b > seq_lens[b] sets
+ * MSA_ERR_SEQ_RANGE and its rows are written as 0.  cu_seqlens_q is not
+ * checked for order: if it is not ascending, a token is attended as a token
+ * of some request whose range holds it, or flagged as above (every read
+ * stays within cu_seqlens_q[0 .. B]).
+ */
+int msa_sparse_prefill(const void *q, const void *kv, const int32_t *block_table,
+                       const int32_t *seq_lens, const int32_t *cu_seqlens_q,
+                       const int32_t *topk, void *workspace, size_t workspace_bytes, void *out,
+                       int B, int T, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                       float k_scale, float v_scale, int num_splits, msa_stream_t stream);
+
+/*
+ * msa_sparse_prefill_select -- msa_sparse_prefill with each (token, KV head)
+ * row's top-16 selected inside the kernel from `scores` [Hkv, T, >= S] (any
+ * element strides), as msa_sparse_decode_select does for decode: the causal
+ * top-k of each query row, with that token's own current block.  `topk`
+ * [T, Hkv, 16] is written.  Arguments and errors as msa_sparse_prefill and
+ * msa_sparse_decode_select.
+ */
+int msa_sparse_prefill_select(const void *q, const void *kv, const int32_t *block_table,
+                              const int32_t *seq_lens, const int32_t *cu_seqlens_q,
+                              const float *scores, int64_t stride_h, int64_t stride_t,
+                              int64_t stride_n, int32_t *topk, void *workspace,
+                              size_t workspace_bytes, void *out, int B, int T, int Hq, int Hkv,
+                              int S, int64_t num_blocks, float sm_scale, float k_scale,
+                              float v_scale, int num_splits, msa_stream_t stream);
+
+/* fp8-query prefill (the vLLM prefill test feeds the attend query_fp8 with
+ * q_scale): q8 and q_scale as the other _q8 entry points. */
+int msa_sparse_prefill_q8(const void *q8, float q_scale, const void *kv,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *cu_seqlens_q, const int32_t *topk, void *workspace,
+                          size_t workspace_bytes, void *out, int B, int T, int Hq, int Hkv, int S,
+                          int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                          int num_splits, msa_stream_t stream);
+int msa_sparse_prefill_select_q8(const void *q8, float q_scale, const void *kv,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 const int32_t *cu_seqlens_q, const float *scores,
+                                 int64_t stride_h, int64_t stride_t, int64_t stride_n,
+                                 int32_t *topk, void *workspace, size_t workspace_bytes,
+                                 void *out, int B, int T, int Hq, int Hkv, int S,
+                                 int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                                 int num_splits, msa_stream_t stream);
+
+/*
  * msa_combine -- stage 4, merge of split-K partials ("fp32 split-K partials"
  * in the TensorRT-LLM flash-decoding commit).  For row r of T*Hq rows, part s
  * holds m_s (max logit in log2 units), l_s = sum 2^(z*log2(e) - m_s) and the

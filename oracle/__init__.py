@@ -234,6 +234,59 @@ def attend_rows(p: Problem, topk_idx, rows, nthreads: int = 0) -> np.ndarray:
     return out
 
 
+def _prefill_requests(seq_lens, cu_seqlens_q):
+    """(b, first token, query length) of each non-empty request of a prefill
+    batch; a request's query tokens are the last q_len of its sequence."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    if cu.shape != (seq_lens.shape[0] + 1,) or cu[0] != 0 or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens_q must be [B + 1], ascending from 0")
+    out = []
+    for b in range(seq_lens.shape[0]):
+        n = int(cu[b + 1] - cu[b])
+        if n > seq_lens[b]:
+            raise ValueError("a request's query length exceeds its sequence length")
+        if n > 0:
+            out.append((b, int(cu[b]), n))
+    return out
+
+
+def attend_prefill(q_bits, kv, block_table, seq_lens, cu_seqlens_q, topk_idx, Hq: int,
+                   Hkv: int, sm_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                   nthreads: int = 0) -> np.ndarray:
+    """Sparse attention of a prefill or chunked-prefill batch, [T, Hq, 128] fp64.
+
+    MiniMaxM3SparsePrefillMetadata on the vLLM pages: request b owns query rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1, and they are the last q_len_b
+    tokens of its seq_lens[b] (context_lens = seq_lens - q_lens), so local
+    token j sits at position seq_lens[b] - q_len_b + j -- the prefill test's
+    visible-page count (seq_len - q_len + local_q) // 128 + 1.  Each request is
+    therefore attend() of a one-request problem with Q = q_len_b."""
+    q_bits = np.asarray(q_bits, dtype=np.uint16)
+    topk_idx = np.asarray(topk_idx, dtype=np.int32)
+    block_table = np.asarray(block_table, dtype=np.int32)
+    out = np.zeros((q_bits.shape[0], Hq, 128), dtype=np.float64)
+    for b, s, n in _prefill_requests(seq_lens, cu_seqlens_q):
+        p = Problem(q_bits[s:s + n], kv, block_table[b:b + 1], np.asarray(seq_lens)[b:b + 1], n,
+                    Hq, Hkv, sm_scale, k_scale, v_scale)
+        out[s:s + n] = attend(p, topk_idx[s:s + n], nthreads)
+    return out
+
+
+def topk_prefill(scores: np.ndarray, seq_lens, cu_seqlens_q, k: int = 16) -> np.ndarray:
+    """Per-token causal top-k of a prefill batch from scores [Hkv, T, S] (any
+    strides): topk() of each request's rows with Q = q_len_b, so each token
+    keeps its own current block.  Rows of empty requests do not exist; the
+    returned [T, Hkv, k] is -1 where no request covers a row."""
+    scores = np.asarray(scores, dtype=np.float64)
+    Hkv, T, _ = scores.shape
+    out = np.full((T, Hkv, k), -1, dtype=np.int32)
+    for b, s, n in _prefill_requests(seq_lens, cu_seqlens_q):
+        out[s:s + n] = topk(scores[:, s:s + n, :], np.asarray(seq_lens, dtype=np.int32)[b:b + 1],
+                            n, k)
+    return out
+
+
 def combine(o, ml) -> np.ndarray:
     """Merge split-softmax parts: o [splits, rows, 128], ml [splits, rows, 2] -> [rows, 128]."""
     o = _c(np.asarray(o, dtype=np.float64), np.float64)

@@ -31,6 +31,33 @@ def to_problem(inp, oracle):
                           inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
 
 
+def prefill_oracle(inp, oracle, topk, nthreads: int = 0) -> np.ndarray:
+    """oracle.attend_prefill on prefill inputs (an fp8 query as in to_problem)."""
+    q, sm_scale = inp.q, inp.sm_scale
+    if q.dtype != torch.bfloat16:
+        q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
+    topk = topk.cpu().numpy() if isinstance(topk, torch.Tensor) else topk
+    return oracle.attend_prefill(q_bits(q), inp.kv.detach().cpu().numpy(),
+                                 inp.block_table.detach().cpu().numpy(),
+                                 inp.seq_lens.detach().cpu().numpy(),
+                                 inp.cu_seqlens_q.detach().cpu().numpy(), topk,
+                                 inp.num_q_heads, inp.num_kv_heads, sm_scale, inp.k_scale,
+                                 inp.v_scale, nthreads)
+
+
+def request_problem(inp, oracle, b: int):
+    """The oracle's problem for request b of a prefill batch alone (Q = its
+    query length, so its tokens sit at the last positions of its sequence)."""
+    q, sm_scale = inp.q, inp.sm_scale
+    if q.dtype != torch.bfloat16:
+        q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
+    s0, n = sum(inp.q_lens[:b]), inp.q_lens[b]
+    return oracle.Problem(q_bits(q[s0:s0 + n]), inp.kv.detach().cpu().numpy(),
+                          inp.block_table[b:b + 1].detach().cpu().numpy(),
+                          inp.seq_lens[b:b + 1].detach().cpu().numpy(), n, inp.num_q_heads,
+                          inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
+
+
 def read_golden_rows(name: str) -> np.ndarray:
     rows = []
     with open(os.path.join(GOLDEN, name)) as f:
@@ -53,7 +80,10 @@ def dense_reference(inp, topk=None):
     softmax(q K^T * sm_scale + causal mask) V over the listed pages (all
     visible pages when topk is None).  Also returns, per (g, token, block), the
     max over the group's heads of the visible logits (the block score)."""
-    B, Q = inp.batch, inp.qlen
+    B = len(inp.seq_lens_list)
+    # one query length per request (prefill inputs), else qlen for every request
+    q_lens = list(inp.q_lens) if inp.q_lens is not None else [inp.qlen] * B
+    first = np.concatenate([[0], np.cumsum(q_lens)]).astype(int)
     Hq, Hkv = inp.num_q_heads, inp.num_kv_heads
     G = Hq // Hkv
     S = inp.stride
@@ -61,9 +91,12 @@ def dense_reference(inp, topk=None):
     K_all = kvf[..., :D] * inp.k_scale
     V_all = kvf[..., D:] * inp.v_scale
     q = inp.q.cpu().to(torch.float64)
+    if inp.q.dtype != torch.bfloat16:     # fp8 query codes, value q * q_scale
+        q = q * inp.q_scale
     bt = inp.block_table.cpu()
-    out = torch.zeros((B * Q, Hq, D), dtype=torch.float64)
-    scores = torch.full((Hkv, B * Q, S), -math.inf, dtype=torch.float64)
+    T = int(first[-1])
+    out = torch.zeros((T, Hq, D), dtype=torch.float64)
+    scores = torch.full((Hkv, T, S), -math.inf, dtype=torch.float64)
     for b, L in enumerate(inp.seq_lens_list):
         n_pages = math.ceil(L / PAGE)
         if n_pages == 0:
@@ -72,8 +105,9 @@ def dense_reference(inp, topk=None):
         for g in range(Hkv):
             K = K_all[pages, g].reshape(n_pages * PAGE, D)
             V = V_all[pages, g].reshape(n_pages * PAGE, D)
+            Q = q_lens[b]
             for j in range(Q):
-                i = b * Q + j
+                i = int(first[b]) + j
                 pos = L - Q + j
                 if pos < 0:
                     continue

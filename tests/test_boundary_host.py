@@ -188,3 +188,40 @@ def test_fp8_query_entry_points_reject_bad_scales(lib):
                                        1.0, 1.0, None) == EINVAL
     assert lib.msa_sparse_decode_select_q8(A, 1.0, A, A, A, None, 0, 0, 1, A, None, 0, A, 16, 4, 64,
                                            4, 8, 100, 0.088, 1.0, 1.0, 1, None) == EINVAL
+
+
+def test_prefill_rejects(lib):
+    f = lib.msa_sparse_prefill
+    ok = dict(kv=A, bt=A, sl=A, cu=A, tk=A, ws=None, wsb=0, out=A, B=3, T=505, Hq=64, Hkv=4,
+              S=9, NB=100, sm=0.088, ks=1.0, vs=1.0, splits=1)
+
+    def call(fn=f, q=(A,), **kw):   # q: (q,) or, for the _q8 entry, (q8, q_scale)
+        a = dict(ok, **kw)
+        return fn(*q, a["kv"], a["bt"], a["sl"], a["cu"], a["tk"], a["ws"], a["wsb"], a["out"],
+                  a["B"], a["T"], a["Hq"], a["Hkv"], a["S"], a["NB"], a["sm"], a["ks"], a["vs"],
+                  a["splits"], None)
+
+    assert call(cu=None) == EINVAL
+    assert call(cu=ctypes.c_void_p((1 << 20) + 2)) == EINVAL     # misaligned cu_seqlens_q
+    assert call(tk=None) == EINVAL
+    assert call(T=-1) == EINVAL
+    assert call(T=(1 << 31) - 1) == EINVAL
+    assert call(B=0) == EINVAL                                    # tokens but no request
+    assert call(T=0) == EINVAL                                    # requests but no token
+    assert call(B=0, T=0) == 0                                    # empty batch
+    assert call(Hq=48) == EINVAL
+    assert call(splits=17) == EINVAL
+    # no query-length bound: a single request of 40000 tokens passes the host checks
+    import torch
+    if not torch.cuda.is_available():
+        assert call(B=1, T=40000) == _native.ECUDA
+    for qs in (0.0, -1.0, float("nan")):
+        assert call(lib.msa_sparse_prefill_q8, (A, qs)) == EINVAL
+    assert call(q=(None,)) == EINVAL
+    g = lib.msa_sparse_prefill_select
+    assert g(A, A, A, A, A, None, 0, 0, 1, A, None, 0, A, 3, 505, 64, 4, 9, 100, 0.088, 1.0, 1.0,
+             1, None) == EINVAL                                   # no scores
+    assert g(A, A, A, A, None, A, 0, 0, 1, A, None, 0, A, 3, 505, 64, 4, 9, 100, 0.088, 1.0, 1.0,
+             1, None) == EINVAL                                   # no cu_seqlens_q
+    assert lib.msa_sparse_prefill_select_q8(A, 0.0, A, A, A, A, A, 0, 0, 1, A, None, 0, A, 3, 505,
+                                            64, 4, 9, 100, 0.088, 1.0, 1.0, 1, None) == EINVAL

@@ -11,8 +11,8 @@ import torch
 import block_sparse_gqa_score_gb300 as msa
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, q_bits,
-                           to_problem)
+from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, prefill_oracle,
+                           q_bits, to_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -419,3 +419,123 @@ def test_fp8_query_select_attend_with_splits():
     assert torch.equal(out, sep)
     assert_out_close(_np(out), oracle.attend(p, _np(tk)), padding_rows(seq_lens, Q))
     assert msa.get_error() == 0
+
+
+# ----------------------------------------------------------------------------- prefill
+
+# The vLLM prefill test's batch in both head geometries (q_lens [300, 128, 77]
+# over seq_lens [300, 640, 1100]: a fresh prompt, then two chunks over cached
+# context), chunks over long contexts, and an empty request with a 70k one.
+PREFILL_CASES = [
+    ([300, 128, 77], [300, 640, 1100], 64, 4),
+    ([300, 128, 77], [300, 640, 1100], 16, 1),
+    ([64, 1, 200, 33], [20000, 9000, 5000, 33], 64, 4),
+    ([5, 0, 7, 1], [500, 300, 900, 70000], 16, 1),
+]
+
+
+@pytest.mark.parametrize("q_lens,seq_lens,Hq,Hkv", PREFILL_CASES)
+@pytest.mark.parametrize("splits", [1, 3])
+def test_prefill_matches_oracle(q_lens, seq_lens, Hq, Hkv, splits):
+    inp = wl.make_prefill(q_lens, seq_lens, Hq, Hkv, seed=121, device=DEV, kv_std=0.5,
+                          kv_scale_mode="amax")
+    topk = wl.draw_topk_varlen(q_lens, seq_lens, Hkv, torch.Generator().manual_seed(12))
+    out = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.cu_seqlens_q,
+                             topk.to(DEV), inp.sm_scale, inp.k_scale, inp.v_scale,
+                             num_splits=splits)
+    assert_out_close(_np(out), prefill_oracle(inp, oracle, topk))
+    assert msa.get_error() == 0
+
+
+def test_prefill_fp8_query_all_visible_pages():
+    """The vLLM prefill test's flow: fp8 query with q_scale, k_scale 0.5 and
+    v_scale 2.0, every causally visible page listed, ending with the token's
+    own page."""
+    q_lens, seq_lens = [300, 128, 77], [300, 640, 1100]
+    for Hq, Hkv in [(64, 4), (16, 1)]:
+        inp = wl.make_prefill(q_lens, seq_lens, Hq, Hkv, seed=122, device=DEV, kv_std=0.25,
+                              fp8_query=True)
+        inp.k_scale, inp.v_scale = 0.5, 2.0
+        topk = wl.all_visible_lists_varlen(q_lens, seq_lens, Hkv, 16)
+        out = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                 inp.cu_seqlens_q, topk.to(DEV), inp.sm_scale, inp.k_scale,
+                                 inp.v_scale, q_scale=inp.q_scale)
+        assert_out_close(_np(out), prefill_oracle(inp, oracle, topk))
+        assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_prefill_with_equal_lengths_is_bit_identical_to_decode(splits):
+    seq_lens, Q, Hq, Hkv = [20000, 9000, 300, 4100], 8, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=123, device=DEV, kv_std=0.5)
+    topk = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(13)).to(DEV)
+    cu = torch.arange(len(seq_lens) + 1, dtype=torch.int32, device=DEV) * Q
+    dec = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, Q, inp.sm_scale,
+                            num_splits=splits)
+    pre = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, cu, topk,
+                             inp.sm_scale, num_splits=splits)
+    assert torch.equal(dec, pre)
+    scores = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale)
+    tk_d, dec_s = msa.sparse_decode_select(inp.q, inp.kv, inp.block_table, inp.seq_lens, scores,
+                                           Q, inp.sm_scale, num_splits=splits)
+    tk_p, pre_s = msa.sparse_prefill_select(inp.q, inp.kv, inp.block_table, inp.seq_lens, cu,
+                                            scores, inp.sm_scale, num_splits=splits)
+    assert torch.equal(tk_d, tk_p) and torch.equal(dec_s, pre_s)
+    assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("S", [40, 700])
+def test_prefill_select_per_token_topk(S):
+    """Per-token causal top-16 from tie-heavy integer scores read through a
+    transposed view: lists bit-exact against the oracle, output identical to
+    msa_sparse_prefill on those lists.  S = 700 takes the selector's path for
+    rows longer than 512 candidates."""
+    g = torch.Generator().manual_seed(S + 3)
+    q_lens = [150, 0, 9, 1]
+    seq_lens = [S * 128 - 7, 200, (S - 30) * 128, 300]
+    inp = wl.make_prefill(q_lens, seq_lens, 32, 2, seed=124, device=DEV, min_stride=S)
+    T = inp.tokens
+    phys = torch.randint(-4, 5, (2, S, T), generator=g).float()
+    scores = phys.to(DEV).transpose(1, 2)                  # [Hkv, T, S] view
+    tk, out = msa.sparse_prefill_select(inp.q, inp.kv, inp.block_table, inp.seq_lens,
+                                        inp.cu_seqlens_q, scores, inp.sm_scale, num_splits=2)
+    want = oracle.topk_prefill(phys.double().numpy().transpose(0, 2, 1), seq_lens,
+                               inp.cu_seqlens_q.cpu().numpy())
+    assert np.array_equal(_np(tk), want)
+    sep = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.cu_seqlens_q, tk,
+                             inp.sm_scale, num_splits=2)
+    assert torch.equal(out, sep)
+    assert msa.get_error() == 0
+
+
+def test_prefill_flags_inconsistent_batches():
+    """Tokens past cu_seqlens_q[B] and a request whose query is longer than
+    its sequence are flagged MSA_ERR_SEQ_RANGE and written as zero rows; every
+    other row is still the oracle's."""
+    q_lens, seq_lens, Hq, Hkv = [40, 9, 30], [3000, 9, 700], 16, 1
+    inp = wl.make_prefill(q_lens, seq_lens, Hq, Hkv, seed=125, device=DEV, kv_std=0.5)
+    topk = wl.draw_topk_varlen(q_lens, seq_lens, Hkv, torch.Generator().manual_seed(14))
+    ref = prefill_oracle(inp, oracle, topk)
+    # cu_seqlens_q ends 10 tokens early: the last request has 20 query tokens
+    # (positions 680 .. 699), and the 10 rows after it belong to no request
+    cu = inp.cu_seqlens_q.clone()
+    cu[-1] -= 10
+    out = _np(msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, cu, topk.to(DEV),
+                                 inp.sm_scale, num_splits=2))
+    assert msa.get_error() & msa._native.ERR_SEQ_RANGE
+    assert np.all(out[69:] == 0.0)
+    short = oracle.attend_prefill(q_bits(inp.q[:69]), inp.kv.cpu().numpy(),
+                                  inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy(),
+                                  cu.cpu().numpy(), topk[:69].numpy(), Hq, Hkv, inp.sm_scale)
+    assert_out_close(out[:69], short)
+    assert np.array_equal(short[:49], ref[:49])
+    # request 1 claims more query tokens than its sequence holds
+    sl = inp.seq_lens.clone()
+    sl[1] = 5
+    out = _np(msa.sparse_prefill(inp.q, inp.kv, inp.block_table, sl, inp.cu_seqlens_q,
+                                 topk.to(DEV), inp.sm_scale))
+    assert msa.get_error() & msa._native.ERR_SEQ_RANGE
+    z = np.zeros(inp.tokens, dtype=bool)
+    z[40:49] = True
+    assert np.all(out[z] == 0.0)
+    assert_out_close(out[~z], ref[~z])

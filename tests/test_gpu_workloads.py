@@ -14,7 +14,8 @@ import torch
 import block_sparse_gqa_score_gb300 as msa
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import SCORE_REL, assert_out_close, assert_scores_close, to_problem
+from tests.helpers import (SCORE_REL, assert_out_close, assert_scores_close, request_problem,
+                           to_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -41,6 +42,9 @@ def test_workload_full_size_sampled(name):
     inp = wl.make_inputs(w, device=DEV)
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     msa.get_error(clear=True)
+    if w.prefill_q:
+        _prefill_full_size(inp, rng)
+        return
     p = to_problem(inp, oracle)
     if w.dense:
         # every visible block: the oracle attends over all-visible lists
@@ -75,6 +79,29 @@ def test_workload_full_size_sampled(name):
            if L - inp.qlen + j < 0]
     if pad:
         assert np.all(out[pad].float().cpu().numpy() == 0.0)
+
+
+def _prefill_full_size(inp, rng):
+    """A prefill batch: msa_sparse_prefill on the drawn per-token lists,
+    sampled (token, head) rows against the oracle of the row's own request."""
+    out = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.cu_seqlens_q,
+                             inp.topk, inp.sm_scale, inp.k_scale, inp.v_scale,
+                             q_scale=inp.q_scale)
+    torch.cuda.synchronize()
+    assert msa.get_error() == 0
+    T, Hq = inp.tokens, inp.num_q_heads
+    o_gpu = out.float().cpu().numpy().reshape(T * Hq, 128).astype(np.float64)
+    topk = inp.topk.cpu().numpy()
+    first = np.concatenate([[0], np.cumsum(inp.q_lens)])
+    rows = rng.choice(T * Hq, size=96, replace=False)
+    o_ref = np.empty((len(rows), 128))
+    for b in range(inp.batch):
+        lo, hi = first[b] * Hq, first[b + 1] * Hq
+        sel = np.nonzero((rows >= lo) & (rows < hi))[0]
+        if len(sel):
+            o_ref[sel] = oracle.attend_rows(request_problem(inp, oracle, b),
+                                            topk[first[b]:first[b + 1]], rows[sel] - lo)
+    assert_out_close(o_gpu[rows], o_ref)
 
 
 @pytest.mark.parametrize("name", ["b16_q4_h64kv4_8k-32k", "b128_q1_h64kv4_lognormal16k_pad10"])

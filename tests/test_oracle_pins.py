@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import dense_reference, q_bits, read_golden_rows, to_problem
+from tests.helpers import (dense_reference, prefill_oracle, q_bits, read_golden_rows,
+                           to_problem)
 
 D = 128
 PAGE = 128
@@ -358,3 +359,97 @@ def test_score_blocks_matches_full_scores():
     for b, g, n in triples:
         rows = slice(b * 3, b * 3 + 3)
         assert np.array_equal(part[g, rows, n], full[g, rows, n])
+
+
+# ----------------------------------------------------------------------------- prefill
+
+# The vLLM prefill test's batch: q_lens [300, 128, 77] over seq_lens
+# [300, 640, 1100] (a fresh prompt, then two chunks over cached context), plus
+# an empty request and single-token chunks of our own.
+PREFILL_CASES = [
+    ([300, 128, 77], [300, 640, 1100], 16, 1),
+    ([5, 0, 1, 40], [700, 300, 129, 40], 8, 2),
+]
+
+
+@pytest.mark.parametrize("q_lens,seq_lens,Hq,Hkv", PREFILL_CASES)
+def test_prefill_equals_dense_causal_attention(q_lens, seq_lens, Hq, Hkv):
+    """With every visible page listed (the prefill test's lists), prefill
+    attention is plain causal attention: token j of request b sees keys
+    0 .. seq_len - q_len + j of its own sequence."""
+    inp = wl.make_prefill(q_lens, seq_lens, Hq, Hkv, seed=21, kv_std=0.7, kv_scale_mode="amax")
+    topk = wl.all_visible_lists_varlen(q_lens, seq_lens, Hkv, 16)
+    ours = prefill_oracle(inp, oracle, topk)
+    ref, _ = dense_reference(inp)
+    np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_sparse_lists_equal_masked_dense():
+    q_lens, seq_lens = [33, 2, 64], [3000, 2100, 64]
+    inp = wl.make_prefill(q_lens, seq_lens, 16, 2, seed=22)
+    topk = wl.draw_topk_varlen(q_lens, seq_lens, 2, torch.Generator().manual_seed(4))
+    ours = prefill_oracle(inp, oracle, topk)
+    ref, _ = dense_reference(inp, topk)
+    np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_token_equals_one_token_decode_at_its_position():
+    """Causality: a prefill token at position pos gives what a one-token
+    decode step of the same sequence cut at pos + 1 gives."""
+    q_lens, seq_lens = [20, 7], [1500, 260]
+    inp = wl.make_prefill(q_lens, seq_lens, 16, 1, seed=23)
+    topk = wl.draw_topk_varlen(q_lens, seq_lens, 1, torch.Generator().manual_seed(5))
+    full = prefill_oracle(inp, oracle, topk)
+    qb = q_bits(inp.q)
+    kv = inp.kv.numpy()
+    bt = inp.block_table.numpy()
+    for i, (b, j) in enumerate([(0, 0), (0, 11), (0, 19), (1, 0), (1, 6)]):
+        row = sum(q_lens[:b]) + j
+        pos = seq_lens[b] - q_lens[b] + j
+        p = oracle.Problem(qb[row:row + 1], kv, bt[b:b + 1], np.array([pos + 1], np.int32), 1,
+                           16, 1, inp.sm_scale, inp.k_scale, inp.v_scale)
+        one = oracle.attend(p, topk[row:row + 1].numpy())
+        assert np.array_equal(one[0], full[row])
+
+
+def test_prefill_with_equal_lengths_is_the_decode_step():
+    seq_lens, Q = [900, 400, 1300], 6
+    inp = wl.make_custom(seq_lens, Q, 16, 2, seed=24)
+    topk = wl.draw_topk_given(seq_lens, Q, 2, torch.Generator().manual_seed(6))
+    dec = oracle.attend(to_problem(inp, oracle), topk.numpy())
+    pre = oracle.attend_prefill(q_bits(inp.q), inp.kv.numpy(), inp.block_table.numpy(),
+                                inp.seq_lens.numpy(), np.arange(4, dtype=np.int32) * Q,
+                                topk.numpy(), 16, 2, inp.sm_scale, inp.k_scale, inp.v_scale)
+    assert np.array_equal(dec, pre)
+    scores = np.random.default_rng(1).integers(-3, 4, (2, 3 * Q, 11)).astype(np.float64)
+    want = oracle.topk(scores, np.array(seq_lens, np.int32), Q)
+    got = oracle.topk_prefill(scores, seq_lens, np.arange(4) * Q)
+    assert np.array_equal(got, want)
+
+
+def test_prefill_topk_keeps_each_tokens_own_block():
+    """Each token of a chunk keeps its own current block, whatever the scores."""
+    seq_lens, q_lens = [3 * PAGE + 10, 20 * PAGE], [2 * PAGE, 3]
+    cu = np.array([0, 2 * PAGE, 2 * PAGE + 3])
+    scores = np.zeros((1, int(cu[-1]), 20))
+    t = oracle.topk_prefill(scores, seq_lens, cu)
+    for b in range(2):
+        for j in range(q_lens[b]):
+            pos = seq_lens[b] - q_lens[b] + j
+            row = t[cu[b] + j, 0]
+            kept = row[row >= 0]
+            assert kept[-1] == pos // PAGE
+            want = min(pos // PAGE + 1, 16)
+            assert len(kept) == want and len(set(kept.tolist())) == want
+
+
+def test_prefill_rejects_inconsistent_lengths():
+    inp = wl.make_prefill([4], [10], 16, 1, seed=25)
+    topk = np.zeros((4, 1, 16), np.int32) - 1
+    with pytest.raises(ValueError):
+        oracle.attend_prefill(q_bits(inp.q), inp.kv.numpy(), inp.block_table.numpy(),
+                              np.array([3], np.int32), np.array([0, 4]), topk, 16, 1, 1.0)
+    with pytest.raises(ValueError):
+        oracle.attend_prefill(q_bits(inp.q), inp.kv.numpy(), inp.block_table.numpy(),
+                              np.array([10, 10], np.int32), np.array([0, 5, 4]), topk, 16, 1,
+                              1.0)
