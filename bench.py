@@ -278,10 +278,11 @@ def run_reference(args, rank, world):
              if inp.seq_lens_list[b] > 0]
 
     given = _given_lists(w, inp)
+    p_score = _score_problem(inp, oracle, p) if p is not None else None
 
     def step(k):
         b, g = units[k % len(units)]
-        _oracle_unit(p, inp, oracle, b, g, cores, given)
+        _oracle_unit(p, inp, oracle, b, g, cores, given, p_score)
         return _unit_tokens(inp, b)
 
     for k in range(args.warmup):
@@ -340,13 +341,26 @@ def _problem(inp, oracle, b=None):
                           inp.num_kv_heads, sm_scale, inp.k_scale, inp.v_scale)
 
 
+def _score_problem(inp, oracle, p):
+    """The problem the oracle scores on: p itself, or (a workload with a K-only
+    index cache) p's query over a packed cache whose K halves are the index-K
+    bytes, with the index cache's scale."""
+    if inp.index_k is None:
+        return p
+    k = inp.index_k.cpu().numpy()
+    kv = np.zeros(k.shape[:3] + (256,), dtype=np.uint8)
+    kv[..., :128] = k
+    return oracle.Problem(p.q, kv, p.block_table, p.seq_lens, p.Q, p.Hq, p.Hkv, p.sm_scale,
+                          inp.index_k_scale, p.v_scale)
+
+
 def _unit_tokens(inp, b) -> float:
     """Query tokens one (request, KV head) unit stands for: its request's / Hkv."""
     Q = inp.q_lens[b] if inp.q_lens is not None else inp.qlen
     return Q / inp.num_kv_heads
 
 
-def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
+def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None, p_score=None):
     """The oracle's whole pipeline for one (request, KV head) unit."""
     Q, G = inp.qlen, inp.num_q_heads // inp.num_kv_heads
     if inp.q_lens is not None:
@@ -359,7 +373,7 @@ def _oracle_unit(p, inp, oracle, b, g, nthreads, topk_given=None):
     cur = (L - 1) // 128
     if topk_given is None:
         triples = [(b, g, n) for n in range(cur + 1)]
-        s = oracle.score_blocks(p, triples, nthreads)
+        s = oracle.score_blocks(p_score if p_score is not None else p, triples, nthreads)
         sub = np.where(np.isnan(s[g:g + 1, b * Q:(b + 1) * Q]), -np.inf,
                        s[g:g + 1, b * Q:(b + 1) * Q])
         t = oracle.topk(sub, np.array([L], dtype=np.int32), Q)       # [Q, 1, 16]
@@ -378,10 +392,11 @@ def cpu_baseline(inp, w, lists, budget_s: float = 12.0):
     cores = oracle.default_threads()
     units = [(b, g) for b in range(inp.batch) for g in range(inp.num_kv_heads)
              if inp.seq_lens_list[b] > 0]
+    p_score = _score_problem(inp, oracle, p) if p is not None else None
     done, tokens = 0, 0.0
     t0 = time.perf_counter()
     for b, g in units:
-        _oracle_unit(p, inp, oracle, b, g, cores, lists)
+        _oracle_unit(p, inp, oracle, b, g, cores, lists, p_score)
         done += 1
         tokens += _unit_tokens(inp, b)
         if time.perf_counter() - t0 > budget_s:
@@ -414,7 +429,8 @@ def run_ours(args, rank, world, local):
 
     # layers: independent KV pools, total >= 4x L2, at least 2
     first = wl.make_inputs(w, device=dev, layer=0)
-    layer_bytes = first.kv.numel() + first.q.numel() * 2
+    layer_bytes = (first.kv.numel() + first.q.numel() * 2
+                   + (first.index_k.numel() if first.index_k is not None else 0))
     n_layers = max(2, math.ceil(4 * l2 / max(layer_bytes, 1)))
     layers = [first] + [wl.make_inputs(w, device=dev, layer=l) for l in range(1, n_layers)]
     T = first.tokens   # every layer has the same request and query lengths
@@ -448,8 +464,11 @@ def run_ours(args, rank, world, local):
                                               inp.topk, inp.qlen, inp.sm_scale, inp.k_scale,
                                               inp.v_scale, out=bf.out, num_splits=bf.num_splits,
                                               workspace=bf.workspace, q_scale=inp.q_scale)]
-        score_call = lambda: msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
-                                       inp.sm_scale, inp.k_scale, scores=bf.scores,
+        # the blocks are scored on the K-only index cache when the workload has one
+        keys, k_sc = ((inp.kv, inp.k_scale) if inp.index_k is None
+                      else (inp.index_k, inp.index_k_scale))
+        score_call = lambda: msa.score(inp.q, keys, inp.block_table, inp.seq_lens, inp.qlen,
+                                       inp.sm_scale, k_sc, scores=bf.scores,
                                        q_scale=inp.q_scale)
         if fused:   # the selection runs inside the attend kernel (msa_sparse_decode_select)
             return [score_call, lambda: None,
@@ -679,6 +698,8 @@ def _to_cpu(inp):
     c.q, c.kv, c.block_table, c.seq_lens = (inp.q.cpu(), inp.kv.cpu(), inp.block_table.cpu(),
                                             inp.seq_lens.cpu())
     c.topk = inp.topk.cpu() if inp.topk is not None else None
+    if inp.index_k is not None:
+        c.index_k = inp.index_k.cpu()
     if inp.cu_seqlens_q is not None:
         c.cu_seqlens_q = inp.cu_seqlens_q.cpu()
     return c
@@ -752,7 +773,8 @@ def _e2e(msa, w, layers, bufs, stream, dev, world, args):
         else:
             msa.decode_step(v["q"], inp.kv, v["block_table"], v["seq_lens"], inp.qlen,
                             inp.sm_scale, inp.k_scale, inp.v_scale, buffers=bf,
-                            q_scale=inp.q_scale)
+                            q_scale=inp.q_scale, index_k=inp.index_k,
+                            index_k_scale=inp.index_k_scale)
 
     def d2h(k):
         l = k % n_layers

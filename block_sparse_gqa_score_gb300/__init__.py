@@ -72,15 +72,18 @@ _KV_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 _FP8_Q = getattr(torch, "float8_e4m3fn", None)
 
 
-def _geometry(q, kv, block_table, seq_lens, qlen: int | None):
-    """Shapes of a step's inputs; q must hold B * qlen tokens (qlen None: any)."""
+def _geometry(q, kv, block_table, seq_lens, qlen: int | None, k_only_ok: bool = False):
+    """Shapes of a step's inputs; q must hold B * qlen tokens (qlen None: any).
+    k_only_ok: kv may also be a K-only cache [num_blocks, Hkv, 128, 128]."""
     _need(q, "q", (torch.bfloat16,) + ((_FP8_Q,) if _FP8_Q is not None else ()))
     dev = q.device
     _need(kv, "kv", _KV_DTYPES, dev)
     _need(block_table, "block_table", (torch.int32,), dev)
     _need(seq_lens, "seq_lens", (torch.int32,), dev)
-    if kv.dim() != 4 or kv.shape[2] != PAGE_SIZE or kv.shape[3] != 2 * HEAD_DIM:
-        raise ValueError("kv must be [num_blocks, Hkv, 128, 256]")
+    if kv.dim() != 4 or kv.shape[2] != PAGE_SIZE or not (
+            kv.shape[3] == 2 * HEAD_DIM or (k_only_ok and kv.shape[3] == HEAD_DIM)):
+        raise ValueError("kv must be [num_blocks, Hkv, 128, 256]"
+                         + (" (or a K-only [num_blocks, Hkv, 128, 128])" if k_only_ok else ""))
     if q.dim() != 3 or q.shape[2] != HEAD_DIM:
         raise ValueError("q must be [T, Hq, 128]")
     if block_table.dim() != 2 or seq_lens.dim() != 1 or block_table.shape[0] != seq_lens.shape[0]:
@@ -115,8 +118,9 @@ def _fp8(q, q_scale: float) -> bool:
 def score(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
           scores: torch.Tensor | None = None, stream=None, q_scale: float = 1.0) -> torch.Tensor:
     """Block scores fp32 [Hkv, T, S] (msa_score; msa_score_q8 for an fp8 q of
-    value q * q_scale)."""
-    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
+    value q * q_scale).  `kv` may be the packed K|V cache [NB, Hkv, 128, 256]
+    or a K-only (index-K) cache [NB, Hkv, 128, 128] (msa_score_kcache)."""
+    dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen, k_only_ok=True)
     if scores is None:
         scores = torch.empty((Hkv, B * qlen, S), dtype=torch.float32, device=dev)
     _need(scores, "scores", (torch.float32,), dev)
@@ -124,10 +128,13 @@ def score(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: flo
         raise ValueError("scores must be [Hkv, T, S]")
     args = (kv.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), scores.data_ptr(), B, qlen,
             Hq, Hkv, S, NB, float(sm_scale), float(k_scale), _stream(dev, stream))
+    k_only = kv.shape[3] == HEAD_DIM
     if _fp8(q, q_scale):
-        st = _lib().msa_score_q8(q.data_ptr(), float(q_scale), *args)
+        f = _lib().msa_score_kcache_q8 if k_only else _lib().msa_score_q8
+        st = f(q.data_ptr(), float(q_scale), *args)
     else:
-        st = _lib().msa_score(q.data_ptr(), *args)
+        f = _lib().msa_score_kcache if k_only else _lib().msa_score
+        st = f(q.data_ptr(), *args)
     _native.check(st, "msa_score")
     return scores
 
@@ -394,16 +401,23 @@ class DecodeBuffers:
 
 def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scale: float = 1.0,
                 v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None,
-                q_scale: float = 1.0):
+                q_scale: float = 1.0, index_k: torch.Tensor | None = None,
+                index_k_scale: float | None = None):
     """score, then selection + attention on one stream, no host sync: in one
     kernel (msa_sparse_decode_select) while rows have at most FUSED_MAX_BLOCKS
     candidate blocks, else msa_topk then msa_sparse_decode (-> combine when
-    split).  Returns (scores, topk, out)."""
+    split).  With `index_k` (a K-only cache [NB, Hkv, 128, 128] on the same
+    block table, scale index_k_scale, default k_scale) the blocks are scored
+    on it instead of kv's K halves.  Returns (scores, topk, out)."""
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if buffers is None:
         buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
-    score(q, kv, block_table, seq_lens, qlen, sm_scale, k_scale, scores=buffers.scores,
-          stream=stream, q_scale=q_scale)
+    if index_k is not None and (index_k.dim() != 4 or index_k.shape[1] != Hkv
+                                or index_k.shape[3] != HEAD_DIM):
+        raise ValueError("index_k must be [num_blocks, Hkv, 128, 128]")
+    score(q, kv if index_k is None else index_k, block_table, seq_lens, qlen, sm_scale,
+          k_scale if index_k is None or index_k_scale is None else index_k_scale,
+          scores=buffers.scores, stream=stream, q_scale=q_scale)
     if fused_selection(S):
         sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale,
                              k_scale, v_scale, topk_out=buffers.topk, out=buffers.out,

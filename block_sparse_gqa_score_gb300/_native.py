@@ -23,7 +23,8 @@ EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode_static", "msa_sparse_decode_select", "msa_dense_splits",
            "msa_dense_decode", "msa_score_q8", "msa_sparse_decode_q8",
            "msa_sparse_decode_select_q8", "msa_dense_decode_q8", "msa_sparse_prefill",
-           "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8")
+           "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
+           "msa_score_kcache", "msa_score_kcache_q8")
 
 _lib = None
 _lock = threading.Lock()
@@ -74,6 +75,9 @@ def load(path: str | None = None):
         lib.msa_sparse_decode_select_q8.argtypes = ([P, f32] +
                                                     lib.msa_sparse_decode_select.argtypes[1:])
         lib.msa_dense_decode_q8.argtypes = [P, f32] + lib.msa_dense_decode.argtypes[1:]
+        # the K-only (index-K) cache scorer: msa_score's arguments
+        lib.msa_score_kcache.argtypes = lib.msa_score.argtypes
+        lib.msa_score_kcache_q8.argtypes = lib.msa_score_q8.argtypes
         # prefill: cu_seqlens_q after seq_lens, (B, T) in place of (B, Q)
         lib.msa_sparse_prefill.argtypes = [P, P, P, P, P, P, P, sz, P, i32, i32, i32, i32, i32,
                                            i64, f32, f32, f32, i32, P]
@@ -91,7 +95,8 @@ def load(path: str | None = None):
                      "msa_sparse_decode_select", "msa_dense_splits", "msa_dense_decode",
                      "msa_score_q8", "msa_sparse_decode_q8", "msa_sparse_decode_select_q8",
                      "msa_dense_decode_q8", "msa_sparse_prefill", "msa_sparse_prefill_select",
-                     "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8"):
+                     "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
+                     "msa_score_kcache", "msa_score_kcache_q8"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -82,16 +82,18 @@ int check_common(const void* q, const void* kv, const int32_t* block_table,
   return MSA_OK;
 }
 
-// 2-D view of the cache as [num_blocks * Hkv * 128 rows, 256 bytes], read in
+// 2-D view of the cache as [num_blocks * Hkv * 128 rows, row_bytes], read in
 // 128 x 128-byte boxes (one K or V half of a page-head) with 128B swizzling.
-// `l2_256` promotes L2 fills to 256 bytes (both halves of a token row, for the
-// attend); the scorer reads K halves only and keeps 128-byte fills so the V
-// halves are not dragged in from DRAM.
+// row_bytes is 256 for the packed K|V cache and 128 for a K-only (index-K)
+// cache, whose boxes at x = 0 are then the same K tiles.  `l2_256` promotes
+// L2 fills to 256 bytes (both halves of a token row, for the attend); the
+// scorer reads K halves only and keeps 128-byte fills so the V halves are not
+// dragged in from DRAM.
 int encode_kv_map(const void* kv, int Hkv, int64_t num_blocks, CUtensorMap* map,
-                  bool l2_256 = true) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2),
+                  bool l2_256 = true, int row_bytes = MSA_HEAD_DIM * 2) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes),
                         static_cast<cuuint64_t>(num_blocks) * Hkv * MSA_PAGE_SIZE};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(MSA_HEAD_DIM * 2)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
   cuuint32_t box[2] = {MSA_HEAD_DIM, MSA_PAGE_SIZE};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides,
@@ -142,10 +144,12 @@ int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
 
 namespace {
 
-// msa_score and msa_score_q8: q_scale > 0 means q is fp8 e4m3 (value q * q_scale).
+// msa_score(_kcache) and their _q8 forms: q_scale > 0 means q is fp8 e4m3
+// (value q * q_scale); k_only: kv is a K-only cache of 128-byte rows.
 int score(const void* q, float q_scale, const void* kv, const int32_t* block_table,
           const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
-          int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream) {
+          int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream,
+          bool k_only = false) {
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
   if (!scores || !aligned(scores, 4) || !finite_pos(sm_scale) || !finite_pos(k_scale) ||
@@ -155,7 +159,9 @@ int score(const void* q, float q_scale, const void* kv, const int32_t* block_tab
   DeviceState* dev;
   if ((st = device_state(&dev)) != MSA_OK) return st;
   CUtensorMap map;
-  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map, /*l2_256=*/false)) != MSA_OK) return st;
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map, /*l2_256=*/false,
+                          k_only ? MSA_HEAD_DIM : 2 * MSA_HEAD_DIM)) != MSA_OK)
+    return st;
   msa::ScoreParams p{};
   p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
   p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
@@ -192,6 +198,22 @@ int msa_score_q8(const void* q8, float q_scale, const void* kv, const int32_t* b
   if (!finite_pos(q_scale)) return MSA_EINVAL;
   return score(q8, q_scale, kv, block_table, seq_lens, scores, B, Q, Hq, Hkv, S, num_blocks,
                sm_scale, k_scale, stream);
+}
+
+int msa_score_kcache(const void* q, const void* k_cache, const int32_t* block_table,
+                     const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
+                     int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream) {
+  return score(q, 0.f, k_cache, block_table, seq_lens, scores, B, Q, Hq, Hkv, S, num_blocks,
+               sm_scale, k_scale, stream, /*k_only=*/true);
+}
+
+int msa_score_kcache_q8(const void* q8, float q_scale, const void* k_cache,
+                        const int32_t* block_table, const int32_t* seq_lens, float* scores,
+                        int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                        float k_scale, msa_stream_t stream) {
+  if (!finite_pos(q_scale)) return MSA_EINVAL;
+  return score(q8, q_scale, k_cache, block_table, seq_lens, scores, B, Q, Hq, Hkv, S, num_blocks,
+               sm_scale, k_scale, stream, /*k_only=*/true);
 }
 
 int msa_topk(const float* scores, int64_t stride_h, int64_t stride_t, int64_t stride_n,

@@ -51,6 +51,8 @@ class Workload:
     # drawn uniformly in [lo, hi] (at most seq_len), each token with its own
     # drawn top-k list (then qlen is unused)
     prefill_q: tuple | None = None
+    # the scorer reads a separate K-only (index-K) cache on the same pages
+    index_k: bool = False
 
     @property
     def tokens(self) -> int:
@@ -65,6 +67,8 @@ class Workload:
              "pipeline": ("dense attend+combine" if self.dense else "attend+combine"
                           if self.topk_given else "score+topk+attend+combine"),
              "query": "fp8 e4m3, per-tensor scale amax/448" if self.fp8_query else "bf16"}
+        if self.index_k:
+            d["scorer_keys"] = "separate K-only index cache [NB, Hkv, 128, 128], fp8"
         if self.prefill_q is not None:
             del d["decode_query_len"]
             d["prefill_query_lens"] = f"uniform {self.prefill_q[0]}-{self.prefill_q[1]}"
@@ -99,6 +103,10 @@ WORKLOADS = {
         # the vLLM CUTLASS decode takes (query_fp8, q_scale)
         Workload("b16_q4_h64kv4_8k-32k_fp8q", 16, 4, 64, 4, "uniform", seed=1007, kv_std=0.5,
                  kv_scale_mode="amax", fp8_query=True, seq_args={"lo": 8192, "hi": 32768}),
+        # the batch-16 step with the blocks scored on a separate K-only cache
+        # (index-K sub-pages) instead of the attend's K
+        Workload("b16_q4_h64kv4_8k-32k_indexk", 16, 4, 64, 4, "uniform", seed=1010, kv_std=0.5,
+                 kv_scale_mode="amax", index_k=True, seq_args={"lo": 8192, "hi": 32768}),
         # chunked prefill on the same model: 4 requests of 8k-32k tokens, each
         # with a 1k-2k query chunk at its end, every token with its own list
         Workload("prefill_b4_chunk1k-2k_h64kv4_8k-32k", 4, 0, 64, 4, "uniform", seed=1009,
@@ -181,6 +189,24 @@ def draw_kv(nb: int, hkv: int, gen: torch.Generator, device, std: float = 1.0,
     kv[..., :HEAD_DIM] = _to_fp8(k.float() / k_scale)
     kv[..., HEAD_DIM:] = _to_fp8(v.float() / v_scale)
     return kv, k_scale, v_scale
+
+
+def draw_index_k(nb: int, hkv: int, gen: torch.Generator, device, std: float = 1.0,
+                 scale_mode: str = "unit"):
+    """A K-only cache [NB, Hkv, 128, 128] as fp8 bytes plus its scale, drawn
+    like draw_kv's K half (N(0, std^2) in bf16, per-tensor scale 1 or
+    amax/448, saturating cast)."""
+    k = torch.randn((max(nb, 1), hkv, PAGE, HEAD_DIM), generator=gen, device=device,
+                    dtype=torch.bfloat16)
+    if std != 1.0:
+        k.mul_(std)
+    if scale_mode == "amax":
+        scale = float(k.abs().max().float()) / FP8_MAX
+    elif scale_mode == "unit":
+        scale = 1.0
+    else:
+        raise ValueError(scale_mode)
+    return _to_fp8(k.float() / scale), scale
 
 
 def draw_topk_varlen(q_lens: list[int], seq_lens: list[int], hkv: int, gen: torch.Generator):
@@ -272,6 +298,9 @@ class StepInputs:
     # rows cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1; qlen is then 0
     q_lens: list | None = None
     cu_seqlens_q: torch.Tensor | None = None   # int32 [B + 1]
+    # a separate K-only cache the scorer reads (index-K sub-pages), same pages
+    index_k: torch.Tensor | None = None        # uint8 [NB, Hkv, 128, 128] (fp8 e4m3 bytes)
+    index_k_scale: float = 1.0
 
     @property
     def batch(self) -> int:
@@ -330,11 +359,16 @@ def make_inputs(w: Workload | str, device="cpu", layer: int = 0,
         qf = q.float()
         q_scale = float(qf.abs().max()) / FP8_MAX
         q = (qf / q_scale).to(torch.float8_e4m3fn)
+    index_k, index_k_scale = None, 1.0
+    if w.index_k:
+        index_k, index_k_scale = draw_index_k(nb, w.num_kv_heads, gen_dev, dev, std=w.kv_std,
+                                              scale_mode=w.kv_scale_mode)
     return StepInputs(q=q, kv=kv, block_table=bt.to(dev),
                       seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=dev),
                       seq_lens_list=list(seq_lens), k_scale=k_scale, v_scale=v_scale,
                       sm_scale=HEAD_DIM ** -0.5, qlen=w.qlen, num_q_heads=w.num_q_heads,
-                      num_kv_heads=w.num_kv_heads, topk=topk, q_scale=q_scale)
+                      num_kv_heads=w.num_kv_heads, topk=topk, q_scale=q_scale,
+                      index_k=index_k, index_k_scale=index_k_scale)
 
 
 def make_custom(seq_lens: list[int], qlen: int, num_q_heads: int, num_kv_heads: int,

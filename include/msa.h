@@ -111,6 +111,27 @@ int msa_score(const void *q, const void *kv, const int32_t *block_table,
               msa_stream_t stream);
 
 /*
+ * msa_score_kcache -- msa_score reading the keys from a K-only cache: the
+ * "index-K sub-pages" that the TensorRT-LLM dense-decode commit says the
+ * MiniMax-M3 cache packs per sparse layer beside the K|V pages.  The pages
+ * give that pool no layout; here it is read as fp8 e4m3 [num_blocks, Hkv, 128,
+ * 128], each page-head the 16 KiB of one K half of a packed page (token row t
+ * at byte offset ((page * Hkv + g) * 128 + t) * 128), addressed through the
+ * same block_table and seq_lens, scaled by k_scale.  Everything else (the
+ * operation, layouts, numerics and errors) is msa_score's, with k_cache in
+ * place of kv; the scores are bit-identical to msa_score's on a packed cache
+ * whose K halves hold the same bytes.  msa_score_kcache_q8 takes the fp8
+ * query as msa_score_q8 does.
+ */
+int msa_score_kcache(const void *q, const void *k_cache, const int32_t *block_table,
+                     const int32_t *seq_lens, float *scores, int B, int Q, int Hq, int Hkv, int S,
+                     int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream);
+int msa_score_kcache_q8(const void *q8, float q_scale, const void *k_cache,
+                        const int32_t *block_table, const int32_t *seq_lens, float *scores,
+                        int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
+                        float k_scale, msa_stream_t stream);
+
+/*
  * msa_topk -- stage 2, the block selector.
  *
  * The selector of TensorRT-LLM PR #17171 reads the score buffer through

@@ -45,6 +45,21 @@ def prefill_oracle(inp, oracle, topk, nthreads: int = 0) -> np.ndarray:
                                  inp.v_scale, nthreads)
 
 
+def index_problem(inp, oracle):
+    """The oracle's problem for scoring on the inputs' K-only (index-K) cache:
+    a packed cache whose K halves are the index-K bytes (V halves zero; the
+    scorer reads no V), with k_scale = index_k_scale."""
+    q, sm_scale = inp.q, inp.sm_scale
+    if q.dtype != torch.bfloat16:
+        q, sm_scale = q.to(torch.bfloat16), inp.sm_scale * inp.q_scale
+    k = inp.index_k.detach().cpu().numpy()
+    kv = np.zeros(k.shape[:3] + (2 * D,), dtype=np.uint8)
+    kv[..., :D] = k
+    return oracle.Problem(q_bits(q), kv, inp.block_table.detach().cpu().numpy(),
+                          inp.seq_lens.detach().cpu().numpy(), inp.qlen, inp.num_q_heads,
+                          inp.num_kv_heads, sm_scale, inp.index_k_scale, inp.v_scale)
+
+
 def request_problem(inp, oracle, b: int):
     """The oracle's problem for request b of a prefill batch alone (Q = its
     query length, so its tokens sit at the last positions of its sequence)."""

@@ -225,3 +225,14 @@ def test_prefill_rejects(lib):
              1, None) == EINVAL                                   # no cu_seqlens_q
     assert lib.msa_sparse_prefill_select_q8(A, 0.0, A, A, A, A, A, 0, 0, 1, A, None, 0, A, 3, 505,
                                             64, 4, 9, 100, 0.088, 1.0, 1.0, 1, None) == EINVAL
+
+
+def test_k_only_cache_scorer_rejects(lib):
+    f = lib.msa_score_kcache
+    assert f(A, None, A, A, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0, None) == EINVAL   # no cache
+    assert f(A, A, A, A, None, 16, 4, 64, 4, 8, 100, 0.088, 1.0, None) == EINVAL   # no scores
+    assert f(A, A, A, A, A, 16, 33, 64, 4, 8, 100, 0.088, 1.0, None) == EINVAL     # qlen 33
+    assert f(A, A, A, A, A, 0, 4, 64, 4, 8, 100, 0.088, 1.0, None) == 0            # empty batch
+    for qs in (0.0, -1.0, float("nan")):
+        assert lib.msa_score_kcache_q8(A, qs, A, A, A, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0,
+                                       None) == EINVAL

@@ -11,8 +11,8 @@ import torch
 import block_sparse_gqa_score_gb300 as msa
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import (assert_out_close, assert_scores_close, padding_rows, prefill_oracle,
-                           q_bits, to_problem)
+from tests.helpers import (assert_out_close, assert_scores_close, index_problem, padding_rows,
+                           prefill_oracle, q_bits, to_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -539,3 +539,53 @@ def test_prefill_flags_inconsistent_batches():
     z[40:49] = True
     assert np.all(out[z] == 0.0)
     assert_out_close(out[~z], ref[~z])
+
+
+# ----------------------------------------------------------------------------- index-K cache
+
+@pytest.mark.parametrize("seq_lens,Q,Hq,Hkv", [([257, 513] * 2, 4, 64, 4),
+                                               ([0, 2, 3, 130, 2048, 2049], 4, 16, 1),
+                                               ([2500, 700], 32, 16, 1),
+                                               ([9000, 300], 16, 32, 2)])
+def test_score_on_a_k_only_cache(seq_lens, Q, Hq, Hkv):
+    """msa_score_kcache: scores on a K-only [NB, Hkv, 128, 128] cache are
+    bit-identical to msa_score on a packed cache holding the same K bytes (any
+    V), for a bf16 and an fp8 query, and match the oracle."""
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=131, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax", min_stride=3)
+    k_only = inp.kv[..., :128].contiguous()
+    got = msa.score(inp.q, k_only, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale)
+    want = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale)
+    assert torch.equal(got, want)
+    inp.index_k, inp.index_k_scale = k_only, inp.k_scale
+    assert_scores_close(_np(got).astype(np.float64), oracle.score(index_problem(inp, oracle)))
+    q8, qs, _ = _fp8_query(inp)
+    got8 = msa.score(q8, k_only, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale,
+                     q_scale=qs)
+    want8 = msa.score(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale,
+                      q_scale=qs)
+    assert torch.equal(got8, want8)
+    assert msa.get_error() == 0
+
+
+def test_decode_step_scores_on_the_index_cache():
+    """decode_step(index_k=...): blocks selected from scores on a separate
+    K-only cache, attended on the K|V cache; the selection is bit-exact
+    against the oracle's given the GPU's scores, the scores and the output
+    match the oracle."""
+    seq_lens, Q, Hq, Hkv = [20000, 9000, 300, 4100], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=132, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    inp.index_k, inp.index_k_scale = wl.draw_index_k(
+        inp.num_blocks, Hkv, torch.Generator(device=DEV).manual_seed(133), DEV, std=0.5,
+        scale_mode="amax")
+    scores, tk, out = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q,
+                                      inp.sm_scale, inp.k_scale, inp.v_scale,
+                                      index_k=inp.index_k, index_k_scale=inp.index_k_scale)
+    s = _np(scores).astype(np.float64)
+    assert_scores_close(s, oracle.score(index_problem(inp, oracle)))
+    want = oracle.topk(s, np.array(seq_lens, dtype=np.int32), Q)
+    assert np.array_equal(_np(tk), want)
+    assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), want),
+                     padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0

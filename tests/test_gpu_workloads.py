@@ -14,8 +14,8 @@ import torch
 import block_sparse_gqa_score_gb300 as msa
 import oracle
 from block_sparse_gqa_score_gb300 import workloads as wl
-from tests.helpers import (SCORE_REL, assert_out_close, assert_scores_close, request_problem,
-                           to_problem)
+from tests.helpers import (SCORE_REL, assert_out_close, assert_scores_close, index_problem,
+                           request_problem, to_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -58,11 +58,14 @@ def test_workload_full_size_sampled(name):
     else:
         scores, topk, out = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens,
                                             inp.qlen, inp.sm_scale, inp.k_scale, inp.v_scale,
-                                            q_scale=inp.q_scale)
+                                            q_scale=inp.q_scale, index_k=inp.index_k,
+                                            index_k_scale=inp.index_k_scale)
         s_gpu = scores.cpu().numpy().astype(np.float64)
-        # scores: sampled blocks against the oracle's definition
+        # scores: sampled blocks against the oracle's definition (on the K-only
+        # index cache when the workload scores on one)
         triples = _sample_triples(inp, rng)
-        s_ref = oracle.score_blocks(p, triples)
+        s_ref = oracle.score_blocks(p if inp.index_k is None else index_problem(inp, oracle),
+                                    triples)
         assert_scores_close(s_gpu, s_ref, mask=~np.isnan(s_ref))
         # selection: bit-exact on every row given the GPU's own scores
         t_ref = oracle.topk(s_gpu, np.array(inp.seq_lens_list, dtype=np.int32), inp.qlen)
