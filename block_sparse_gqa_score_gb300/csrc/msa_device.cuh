@@ -118,12 +118,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned pari
 }
 
 // Wait for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
-// Waiting warps sleep inside try_wait instead of spinning, so they leave the
-// issue slots to the warps doing work.  Returns false on timeout (the caller
-// flags MSA_ERR_TIMEOUT and bails out).
+// The first two tries carry no suspend-time hint: on the kernels' per-page
+// hand-offs (TMA -> MMA -> softmax -> MMA) they return sooner after the phase
+// completes than a hinted try does (the batch-16, qlen-4 step 69.3 vs 70.3 us,
+// its attend alone 24.5 vs 25.1 us).  Longer waits then sleep inside try_wait
+// with a 1 ms hint, leaving the issue slots to the warps doing work (polling
+// with test_wait instead cost 17 us per step).  Returns false on timeout (the
+// caller flags MSA_ERR_TIMEOUT and bails out).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
   constexpr unsigned kHintNs = 1000000u;  // re-check the time limit every 1 ms at most
-  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+  if (mbar_try_wait(bar, parity) || mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
