@@ -52,3 +52,56 @@ def test_mutant_is_caught(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+
+
+# The prefill routines compose the decode routines per request in Python
+# (oracle/__init__.py); their plausible mistakes are planted in a copy of that
+# module, which a child process loads as `oracle` before running the prefill
+# pins against the unmodified C library.
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
+PY_MUTANTS = {
+    "unmodified": None,
+    # the chunk placed at the start of its sequence instead of its end
+    "prefill_tokens_at_sequence_start": (
+        "np.asarray(seq_lens)[b:b + 1], n,",
+        "np.minimum(np.asarray(seq_lens)[b:b + 1], n), n,"),
+    # a request's queries taken in reverse token order
+    "prefill_query_rows_reversed": (
+        "p = Problem(q_bits[s:s + n], kv,",
+        "p = Problem(np.ascontiguousarray(q_bits[s:s + n][::-1]), kv,"),
+    # the selection made as if the chunk started the sequence
+    "prefill_selection_at_sequence_start": (
+        "np.asarray(seq_lens, dtype=np.int32)[b:b + 1],\n                            n, k)",
+        "np.minimum(np.asarray(seq_lens, dtype=np.int32)[b:b + 1], n),\n"
+        "                            n, k)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_prefill_mutant_is_caught(name, tmp_path):
+    import oracle
+    src = open(PY_SRC).read()
+    if PY_MUTANTS[name] is not None:
+        old, new = PY_MUTANTS[name]
+        assert src.count(old) == 1, f"mutation site for {name} not found"
+        src = src.replace(old, new)
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(src)
+    script = (
+        "import importlib.util, sys\n"
+        f"spec = importlib.util.spec_from_file_location('oracle', {str(pkg / '__init__.py')!r},\n"
+        f"    submodule_search_locations=[{str(pkg)!r}])\n"
+        "m = importlib.util.module_from_spec(spec)\n"
+        "sys.modules['oracle'] = m\n"
+        "spec.loader.exec_module(m)\n"
+        "import pytest\n"
+        "sys.exit(pytest.main(['-x', '-q', '-p', 'no:cacheprovider', '-k', 'prefill',\n"
+        f"    {os.path.join(ROOT, 'tests', 'test_oracle_pins.py')!r}]))\n")
+    env = dict(os.environ, MSA_ORACLE_LIB=oracle.build())
+    r = subprocess.run([sys.executable, "-c", script], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    if PY_MUTANTS[name] is None:     # the harness itself: an unmodified copy passes every pin
+        assert r.returncode == 0, r.stdout[-2000:]
+    else:                            # a pin fails (exit status 1), not the harness
+        assert r.returncode == 1, f"mutant {name}: status {r.returncode}\n{r.stdout[-2000:]}"
