@@ -289,8 +289,8 @@ int msa_dense_decode_q8(const void *q8, float q_scale, const void *kv,
  *
  *   pos = context_len_b + j,  context_len_b = seq_lens[b] - q_len_b,
  *
- * (the vLLM prefill test's visible-page count (seq_len - q_len + local_q) /
- * 128 + 1).  Each token attends the blocks of its own list topk[i, g, :]
+ * so it sees pages 0 .. pos / 128, as the vLLM prefill test counts them.
+ * Each token attends the blocks of its own list topk[i, g, :]
  * [T, Hkv, 16] with the causal bound 128*n + t <= pos; the operation, output
  * layout [T, Hq, 128], numerics and device errors are msa_sparse_decode's,
  * which this call equals when every request has the same query length.

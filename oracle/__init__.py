@@ -258,10 +258,10 @@ def attend_prefill(q_bits, kv, block_table, seq_lens, cu_seqlens_q, topk_idx, Hq
 
     MiniMaxM3SparsePrefillMetadata on the vLLM pages: request b owns query rows
     cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1, and they are the last q_len_b
-    tokens of its seq_lens[b] (context_lens = seq_lens - q_lens), so local
-    token j sits at position seq_lens[b] - q_len_b + j -- the prefill test's
-    visible-page count (seq_len - q_len + local_q) // 128 + 1.  Each request is
-    therefore attend() of a one-request problem with Q = q_len_b."""
+    tokens of its seq_lens[b] (the cached context being seq_lens[b] -
+    q_len_b), so local token j sits at position seq_lens[b] - q_len_b + j and
+    sees pages 0 .. pos / 128, as the vLLM prefill test counts them.  Each
+    request is therefore attend() of a one-request problem with Q = q_len_b."""
     q_bits = np.asarray(q_bits, dtype=np.uint16)
     topk_idx = np.asarray(topk_idx, dtype=np.int32)
     block_table = np.asarray(block_table, dtype=np.int32)
