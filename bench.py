@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -189,11 +190,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": where}
 
 
+def _code_only(src: str) -> str:
+    """A CUDA source without its comments and blank space: what the compiler
+    sees, so that an edit to a comment leaves a kernel's digest unchanged."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.strip() for line in src.splitlines() if line.strip())
+
+
 def _source_digest(*names) -> str:
+    """Digest of a kernel's sources (code only), recorded with each ncu summary
+    under profiles/: a summary whose digest differs describes other code."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "block_sparse_gqa_score_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "block_sparse_gqa_score_gb300", "csrc", n)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

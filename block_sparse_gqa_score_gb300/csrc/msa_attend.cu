@@ -3,9 +3,8 @@
 // Operation: minimax_m3_sparse_attn_decode / msa_cutlass_sparse_decode on the
 // vLLM MiniMax-M3 pages: each query row attends only the tokens of the <= 16
 // blocks its KV head's top-k list names, causally limited to pos = seq_len -
-// Q + j; padding rows give zero (TensorRT-LLM PR #17171, flash-decoding
-// commit: "zeroed (not NaN) output for graph padding rows", fp32 split-K
-// partials).
+// Q + j; padding rows come out as zeros rather than NaN, and split parts are
+// merged from fp32 partials (TensorRT-LLM PR #17171, flash-decoding commit).
 //
 // Design (sm_103a, tcgen05): one CTA per (query token, KV head, split).  The
 // token's 16 query heads are the N = 16 columns of two tensor-core products
@@ -37,8 +36,10 @@
 // dense-decode commit: the first layers attend the whole page table) a range
 // of consecutive visible blocks.  An fp8 query (value q8 * q_scale, as
 // msa_cutlass_sparse_decode takes it) goes into the hi part as stored, with a
-// zero lo part.  Dense decode and the fp8 query are template flags, so the
-// bf16 list-mode kernel carries none of their branches.
+// zero lo part.  Prefill batches (one query length per request, cu_seqlens_q)
+// map each token to its request by a warp-wide search and then run as decode
+// tokens.  Dense decode, the fp8 query and prefill batches are template
+// flags, so the bf16 list-mode decode kernel carries none of their branches.
 #include "msa_device.cuh"
 #include "msa_launch.h"
 #include "msa_select.cuh"
