@@ -3,7 +3,7 @@
 One decode step of MiniMax-M3-style indexer-selected sparse attention, as the
 vLLM MiniMax-M3 sparse attention pages and TensorRT-LLM PR #17171 describe it:
 
-  score()          per-block causal max of scaled q.k over each KV head's group
+  score()          each block's largest visible scaled q.k over a KV head's query heads
   topk()           top-16 blocks (current block kept, ties to the lower index)
   sparse_decode()  split-K attention over the selected pages (+ merge)
   sparse_prefill() the same attend for prefill batches (one query length per

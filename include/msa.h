@@ -5,8 +5,8 @@
  * KV cache, as the vLLM MiniMax-M3 sparse attention pages and the
  * TensorRT-LLM PR #17171 "Custom decode kernels for MinimaxM3" describe it:
  *
- *   msa_score          per-block causal max of scaled q.k over each KV head's
- *                      query-head group                        (stage 1)
+ *   msa_score          each block's largest visible scaled q.k over the
+ *                      query heads of its KV head              (stage 1)
  *   msa_topk           top-16 block selection                  (stage 2)
  *   msa_sparse_decode  split-K attention over the selected pages (stage 3)
  *   msa_combine        merge of the split-K partials            (stage 4)
@@ -85,9 +85,9 @@ typedef struct CUstream_st *msa_stream_t;
 /*
  * msa_score -- stage 1, the block scorer.
  *
- * Defined by the scorer commit of TensorRT-LLM PR #17171 ("the same
- * per-block causal max of Q.K", written in [head, token, block] order): for
- * every KV head g, query token i and logical block n < S,
+ * Defined by the scorer commit of TensorRT-LLM PR #17171 (each block's
+ * largest q.k under the causal mask, stored head-major, then token, then
+ * block): for every KV head g, query token i and logical block n < S,
  *
  *   scores[g, i, n] = max over query heads h of group g and over tokens t of
  *                     block n with 128*n + t <= pos(i) of

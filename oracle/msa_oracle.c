@@ -24,9 +24,9 @@
  *          ids, -1 padding), the interleaved-cache test (float8_e4m3fn K|V
  *          concatenated on the content dim, block_table [batch, stride]).
  *   [PR]   TensorRT-LLM PR #17171 "Custom decode kernels for MinimaxM3":
- *          the scorer commit (per-block causal max of Q.K, written as
- *          [head, token, block]; the selector takes arbitrary strides) and the
- *          flash-decoding commit (zeroed, not NaN, output for padding rows).
+ *          the scorer commit (each block's largest q.k under the causal
+ *          mask, stored head, token, block; the selector reads any strides)
+ *          and the flash-decoding commit (padding rows are written as zeros).
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes): the group of query head h is g = h / G with G = Hq / Hkv; the
@@ -420,7 +420,7 @@ int orc_topk(const double *scores, int64_t stride_h, int64_t stride_t, int64_t s
  * with M = max_t z_t (the usual max-subtracted two-pass form), K scaled by
  * k_scale and V by v_scale, no softcap, sink or output scale ([CUT]
  * o_scale = 1.0).  An empty key set or a padding row gives O = 0 ([PR]
- * zeroed, not NaN, output for padding rows).  A listed block outside
+ * flash-decoding commit: such rows are written as zeros).  A listed block outside
  * [0, cur] or listed twice is a precondition violation (status 2). */
 
 typedef struct {
