@@ -279,6 +279,7 @@ DENSE_CASES = [
     ([2500, 700], 32, 16, 1),                     # qlen at its upper bound
     ([20000, 9000, 40000], 4, 64, 4),             # 16 splits of 20 blocks
     ([70000], 2, 16, 1),                          # blocks past the prologue's table copy
+    ([262144], 1, 16, 1),                         # the longest table: 16 splits of 128 blocks
 ]
 
 
@@ -588,4 +589,21 @@ def test_decode_step_scores_on_the_index_cache():
     assert np.array_equal(_np(tk), want)
     assert_out_close(_np(out), oracle.attend(to_problem(inp, oracle), want),
                      padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("B", [100, 1100])
+def test_prefill_many_requests(B):
+    """More requests than a warp has lanes: the token -> request search takes
+    two (100 requests) and three (1100) rounds.  Ragged query lengths with
+    empty requests and fresh prompts."""
+    g = torch.Generator().manual_seed(B)
+    seq_lens = torch.randint(1, 3000, (B,), generator=g).tolist()
+    q_lens = [min(L, int(n)) for L, n in zip(seq_lens, torch.randint(0, 6, (B,), generator=g))]
+    q_lens[3] = seq_lens[3]                                  # a whole prompt
+    inp = wl.make_prefill(q_lens, seq_lens, 16, 1, seed=126, device=DEV, kv_std=0.5)
+    topk = wl.draw_topk_varlen(q_lens, seq_lens, 1, torch.Generator().manual_seed(15))
+    out = msa.sparse_prefill(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.cu_seqlens_q,
+                             topk.to(DEV), inp.sm_scale, num_splits=2)
+    assert_out_close(_np(out), prefill_oracle(inp, oracle, topk))
     assert msa.get_error() == 0
