@@ -38,7 +38,7 @@ def _rank_main(rank: int, world: int, port: int, out):
 
 def test_two_gloo_ranks_take_the_max_over_ranks():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork of a threaded test process
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}
 
