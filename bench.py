@@ -52,15 +52,25 @@ PROFILES = os.path.join(ROOT, "profiles")
 # ----------------------------------------------------------------------------- helpers
 
 def _args():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=None)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--graph-chunk", type=int, default=250)
+    from block_sparse_gqa_score_gb300 import workloads as wl
+    ap = argparse.ArgumentParser(
+        description="One JSON line: query tokens/s per layer of a workload's step, with the "
+                    "dominant kernel's roofline, the end-to-end figure and the CPU oracle's.")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks, one GPU each (N > 1: launched under torchrun, replicas)")
+    ap.add_argument("--steps", type=int, default=2000, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=50, help="untimed warm-up steps (at least 3 for a valid measurement)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="ours: the CUDA library; reference: the fp64 CPU oracle, one "
+                         "(request, KV head) unit per step")
+    ap.add_argument("--workload", default=None, choices=sorted(wl.WORKLOADS),
+                    help=f"default: {wl.HEADLINE}")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end measurement (host copies, public API)")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the CPU oracle beside the line")
+    ap.add_argument("--graph-chunk", type=int, default=250,
+                    help="steps captured per CUDA graph in the timed region")
     return ap.parse_args()
 
 
