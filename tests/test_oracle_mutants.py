@@ -21,6 +21,8 @@ MUTANTS = {
     "value_scale_dropped": ("return orc_e4m3(row[ORC_D + d]) * p->v_scale;",
                             "return orc_e4m3(row[ORC_D + d]);"),
     "key_scale_dropped": ("return orc_e4m3(row[d]) * p->k_scale;", "return orc_e4m3(row[d]);"),
+    "key_reads_value_half": ("return orc_e4m3(row[d]) * p->k_scale;",
+                             "return orc_e4m3(row[ORC_D + d]) * p->k_scale;"),
     "sm_scale_dropped": ("return p->sm_scale * acc;", "return acc;"),
     "ties_to_higher_index": ("return (x->block < y->block) ? -1 : (x->block > y->block) ? 1 : 0;",
                              "return (x->block < y->block) ? 1 : (x->block > y->block) ? -1 : 0;"),

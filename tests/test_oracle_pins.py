@@ -453,3 +453,17 @@ def test_prefill_rejects_inconsistent_lengths():
         oracle.attend_prefill(q_bits(inp.q), inp.kv.numpy(), inp.block_table.numpy(),
                               np.array([10, 10], np.int32), np.array([0, 5, 4]), topk, 16, 1,
                               1.0)
+
+
+# ----------------------------------------------------------------------------- index-K cache
+
+def test_score_ignores_the_value_half():
+    """The scores depend on the K half of each page row only: replacing every
+    V byte leaves them bit-identical (the premise of scoring on a K-only
+    cache laid into the K halves of a packed one)."""
+    inp = wl.make_custom([3000, 700], 4, 16, 2, seed=31, kv_std=0.5, kv_scale_mode="amax")
+    ref = oracle.score(to_problem(inp, oracle))
+    other = inp.kv.clone()
+    other[..., D:] = torch.randint(0, 0x7F, other[..., D:].shape, dtype=torch.uint8)
+    inp.kv = other
+    assert np.array_equal(oracle.score(to_problem(inp, oracle)), ref)
