@@ -12,6 +12,9 @@
  *   msa_combine        merge of the split-K partials            (stage 4)
  *   msa_sparse_decode_select  stages 2 and 3 in one kernel
  *   msa_dense_decode   attention over every visible block (dense layers)
+ *   msa_sparse_prefill(_select)  the attend for prefill and chunked-prefill
+ *                      batches: one query length per request (cu_seqlens_q)
+ *   msa_score_kcache   stage 1 on a separate K-only (index-K) cache
  *   msa_*_q8           the same with an fp8 query and a per-tensor q_scale
  *
  * Conventions shared by every entry point
@@ -23,7 +26,8 @@
  *    legacy default stream) and returns without waiting.  No call
  *    synchronises the host except msa_get_error.
  *  - Sizes: B requests, Q = decode_query_len query tokens per request,
- *    T = B*Q query tokens ordered request-major (token i = b*Q + j),
+ *    T = B*Q query tokens ordered request-major (token i = b*Q + j; the
+ *    prefill entry points take T and cu_seqlens_q instead of Q),
  *    Hq query heads and Hkv KV heads with Hq = 16 * Hkv (query head h belongs
  *    to KV head g = h / 16), head size 128, page size 128 tokens, S = the
  *    block_table row stride (max logical blocks per request), num_blocks =
