@@ -41,7 +41,7 @@ __all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "sparse_pre
            "sparse_prefill_select", "dense_decode", "dense_splits",
            "combine", "decode_step",
            "fused_selection", "FUSED_MAX_BLOCKS", "workspace_bytes",
-           "choose_splits", "get_error", "DecodeBuffers", "MSAError"]
+           "choose_splits", "get_error", "set_input_overlap", "DecodeBuffers", "MSAError"]
 
 
 def _lib():
@@ -403,8 +403,9 @@ def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scal
                 v_scale: float = 1.0, buffers: DecodeBuffers | None = None, stream=None,
                 q_scale: float = 1.0, index_k: torch.Tensor | None = None,
                 index_k_scale: float | None = None):
-    """score, then selection + attention on one stream, no host sync: in one
-    kernel (msa_sparse_decode_select) while rows have at most FUSED_MAX_BLOCKS
+    """One decode step in one library call (msa_decode_step): score, then
+    selection + attention on one stream, no host sync -- in one kernel
+    (msa_sparse_decode_select) while rows have at most FUSED_MAX_BLOCKS
     candidate blocks, else msa_topk then msa_sparse_decode (-> combine when
     split).  With `index_k` (a K-only cache [NB, Hkv, 128, 128] on the same
     block table, scale index_k_scale, default k_scale) the blocks are scored
@@ -412,23 +413,39 @@ def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scal
     dev, B, S, Hq, Hkv, NB = _geometry(q, kv, block_table, seq_lens, qlen)
     if buffers is None:
         buffers = DecodeBuffers.allocate(B, qlen, Hq, Hkv, S, dev)
-    if index_k is not None and (index_k.dim() != 4 or index_k.shape[1] != Hkv
-                                or index_k.shape[3] != HEAD_DIM):
-        raise ValueError("index_k must be [num_blocks, Hkv, 128, 128]")
-    score(q, kv if index_k is None else index_k, block_table, seq_lens, qlen, sm_scale,
-          k_scale if index_k is None or index_k_scale is None else index_k_scale,
-          scores=buffers.scores, stream=stream, q_scale=q_scale)
-    if fused_selection(S):
-        sparse_decode_select(q, kv, block_table, seq_lens, buffers.scores, qlen, sm_scale,
-                             k_scale, v_scale, topk_out=buffers.topk, out=buffers.out,
-                             num_splits=buffers.num_splits, workspace=buffers.workspace,
-                             stream=stream, q_scale=q_scale)
-    else:
-        topk(buffers.scores, seq_lens, qlen, out=buffers.topk, stream=stream)
-        sparse_decode(q, kv, block_table, seq_lens, buffers.topk, qlen, sm_scale, k_scale,
-                      v_scale, out=buffers.out, num_splits=buffers.num_splits,
-                      workspace=buffers.workspace, stream=stream, q_scale=q_scale)
-    return buffers.scores, buffers.topk, buffers.out
+    if index_k is not None:
+        _need(index_k, "index_k", _KV_DTYPES, dev)
+        if (index_k.dim() != 4 or index_k.shape[1] != Hkv or index_k.shape[2] != PAGE_SIZE
+                or index_k.shape[3] != HEAD_DIM or index_k.shape[0] != NB):
+            raise ValueError("index_k must be [num_blocks, Hkv, 128, 128]")
+    bf = buffers
+    _need(bf.scores, "scores", (torch.float32,), dev)
+    _need(bf.topk, "topk", (torch.int32,), dev)
+    _need(bf.out, "out", (torch.bfloat16,), dev)
+    if (tuple(bf.scores.shape) != (Hkv, B * qlen, S) or tuple(bf.topk.shape) != (B * qlen, Hkv, TOPK)
+            or tuple(bf.out.shape) != tuple(q.shape)):
+        raise ValueError("buffers do not match the step's shapes")
+    ws = bf.workspace
+    ws_ptr = ws.data_ptr() if ws is not None else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    fp8 = _fp8(q, q_scale)
+    ik_scale = (k_scale if index_k_scale is None else index_k_scale) if index_k is not None else 0.0
+    st = _lib().msa_decode_step(
+        q.data_ptr(), float(q_scale) if fp8 else 0.0, kv.data_ptr(),
+        index_k.data_ptr() if index_k is not None else None, float(ik_scale),
+        block_table.data_ptr(), seq_lens.data_ptr(), bf.scores.data_ptr(), bf.topk.data_ptr(),
+        ws_ptr, ws_bytes, bf.out.data_ptr(), B, qlen, Hq, Hkv, S, NB, float(sm_scale),
+        float(k_scale), float(v_scale), bf.num_splits, _stream(dev, stream))
+    _native.check(st, "msa_decode_step")
+    return bf.scores, bf.topk, bf.out
+
+
+def set_input_overlap(enable: bool) -> bool:
+    """msa_set_input_overlap: let the first kernel of every library call start
+    before the previous kernel on its stream has finished (only safe when that
+    kernel wrote none of the call's inputs, e.g. another library call).  Off
+    by default.  Returns the previous setting."""
+    return bool(_lib().msa_set_input_overlap(1 if enable else 0))
 
 
 def get_error(clear: bool = True) -> int:

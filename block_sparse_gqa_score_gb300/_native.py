@@ -24,7 +24,8 @@ EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_dense_decode", "msa_score_q8", "msa_sparse_decode_q8",
            "msa_sparse_decode_select_q8", "msa_dense_decode_q8", "msa_sparse_prefill",
            "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
-           "msa_score_kcache", "msa_score_kcache_q8")
+           "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
+           "msa_set_input_overlap")
 
 _lib = None
 _lock = threading.Lock()
@@ -87,6 +88,10 @@ def load(path: str | None = None):
         lib.msa_sparse_prefill_q8.argtypes = [P, f32] + lib.msa_sparse_prefill.argtypes[1:]
         lib.msa_sparse_prefill_select_q8.argtypes = ([P, f32] +
                                                      lib.msa_sparse_prefill_select.argtypes[1:])
+        # the whole step: (q, q_scale, kv, index_k, index_k_scale, ...)
+        lib.msa_decode_step.argtypes = [P, f32, P, P, f32, P, P, P, P, P, sz, P, i32, i32, i32,
+                                        i32, i32, i64, f32, f32, f32, i32, P]
+        lib.msa_set_input_overlap.argtypes = [i32]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
@@ -96,7 +101,8 @@ def load(path: str | None = None):
                      "msa_score_q8", "msa_sparse_decode_q8", "msa_sparse_decode_select_q8",
                      "msa_dense_decode_q8", "msa_sparse_prefill", "msa_sparse_prefill_select",
                      "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
-                     "msa_score_kcache", "msa_score_kcache_q8"):
+                     "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
+                     "msa_set_input_overlap"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -8,6 +8,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "msa.h"
@@ -29,6 +30,11 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+// msa_set_input_overlap: whether each entry point's first kernel may start
+// before the previous kernel on its stream has finished (off by default)
+std::atomic<int> g_input_overlap{0};
+
+bool input_overlap() { return g_input_overlap.load(std::memory_order_relaxed) != 0; }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Set-up for the current device, done once: resolves the device address of the
@@ -144,12 +150,13 @@ int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
 
 namespace {
 
-// msa_score(_kcache) and their _q8 forms: q_scale > 0 means q is fp8 e4m3
-// (value q * q_scale); k_only: kv is a K-only cache of 128-byte rows.
-int score(const void* q, float q_scale, const void* kv, const int32_t* block_table,
-          const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
-          int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream,
-          bool k_only = false) {
+// Checks and parameter block of msa_score(_kcache) and their _q8 forms:
+// q_scale > 0 means q is fp8 e4m3 (value q * q_scale); k_only: kv is a K-only
+// cache of 128-byte rows.  Nothing is enqueued.
+int prepare_score(const void* q, float q_scale, const void* kv, const int32_t* block_table,
+                  const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
+                  int64_t num_blocks, float sm_scale, float k_scale, bool k_only,
+                  msa::ScoreParams* p, CUtensorMap* map) {
   int st = check_common(q, kv, block_table, seq_lens, B, Q, Hq, Hkv, S, num_blocks);
   if (st != MSA_OK) return st;
   if (!scores || !aligned(scores, 4) || !finite_pos(sm_scale) || !finite_pos(k_scale) ||
@@ -158,27 +165,39 @@ int score(const void* q, float q_scale, const void* kv, const int32_t* block_tab
   if (B == 0) return MSA_OK;
   DeviceState* dev;
   if ((st = device_state(&dev)) != MSA_OK) return st;
-  CUtensorMap map;
-  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map, /*l2_256=*/false,
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, map, /*l2_256=*/false,
                           k_only ? MSA_HEAD_DIM : 2 * MSA_HEAD_DIM)) != MSA_OK)
     return st;
-  msa::ScoreParams p{};
-  p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
-  p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
-  p.q_scale = q_scale;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.scores = scores;
-  p.err = dev->err;
-  p.B = B;
-  p.Q = Q;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.S = S;
-  p.ctas = dev->sm_count;
-  p.num_blocks = num_blocks;
-  p.scale = sm_scale * k_scale;
-  return from_cuda(msa::launch_score(map, p, reinterpret_cast<cudaStream_t>(stream)));
+  *p = msa::ScoreParams{};
+  p->q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
+  p->q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
+  p->q_scale = q_scale;
+  p->block_table = block_table;
+  p->seq_lens = seq_lens;
+  p->scores = scores;
+  p->err = dev->err;
+  p->B = B;
+  p->Q = Q;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->S = S;
+  p->ctas = dev->sm_count;
+  p->num_blocks = num_blocks;
+  p->scale = sm_scale * k_scale;
+  return MSA_OK;
+}
+
+int score(const void* q, float q_scale, const void* kv, const int32_t* block_table,
+          const int32_t* seq_lens, float* scores, int B, int Q, int Hq, int Hkv, int S,
+          int64_t num_blocks, float sm_scale, float k_scale, msa_stream_t stream,
+          bool k_only = false) {
+  msa::ScoreParams p;
+  CUtensorMap map;
+  const int st = prepare_score(q, q_scale, kv, block_table, seq_lens, scores, B, Q, Hq, Hkv, S,
+                               num_blocks, sm_scale, k_scale, k_only, &p, &map);
+  if (st != MSA_OK || B == 0) return st;
+  return from_cuda(
+      msa::launch_score(map, p, reinterpret_cast<cudaStream_t>(stream), input_overlap()));
 }
 
 }  // namespace
@@ -240,7 +259,7 @@ int msa_topk(const float* scores, int64_t stride_h, int64_t stride_t, int64_t st
   p.Q = Q;
   p.Hkv = Hkv;
   p.S = S;
-  return from_cuda(msa::launch_topk(p, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(msa::launch_topk(p, reinterpret_cast<cudaStream_t>(stream), input_overlap()));
 }
 
 int msa_combine(const void* workspace, void* out, int T, int Hq, int num_splits,
@@ -252,7 +271,8 @@ int msa_combine(const void* workspace, void* out, int T, int Hq, int num_splits,
   const float* part_o = static_cast<const float*>(workspace);
   const float* part_ml = part_o + static_cast<int64_t>(num_splits) * rows * MSA_HEAD_DIM;
   return from_cuda(msa::launch_combine(part_o, part_ml, static_cast<uint16_t*>(out), rows,
-                                       num_splits, reinterpret_cast<cudaStream_t>(stream)));
+                                       num_splits, reinterpret_cast<cudaStream_t>(stream),
+                                       input_overlap()));
 }
 
 }  // extern "C"
@@ -269,19 +289,28 @@ void dense_split(int S, int* nsplit, int* span) {
   *span = (S + *nsplit - 1) / *nsplit;
 }
 
-// msa_sparse_decode, msa_sparse_decode_select and msa_dense_decode: `scores`
-// null means `topk` is the input list; otherwise the lists are selected from
-// the strided scores inside the attend kernel and written to `topk`.
-// dense_span > 0: no list, every visible block (msa_dense_decode).
-// cu_q non-null: a prefill-style batch of T tokens, request b owning tokens
-// [cu_q[b], cu_q[b + 1]) (msa_sparse_prefill); Q is then unused.
-int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
-                  const int32_t* seq_lens, const float* scores, int64_t stride_h,
-                  int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
-                  size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
-                  int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
-                  int num_splits, msa_stream_t stream, int dense_span = 0, float q_scale = 0.f,
-                  const int32_t* cu_q = nullptr, int T = 0) {
+// An attend launch, checked and ready to enqueue.
+struct AttendLaunch {
+  msa::AttendParams p;
+  CUtensorMap map;
+  int64_t rows;  // output rows (tokens x query heads)
+};
+
+// Checks and parameter block of msa_sparse_decode, msa_sparse_decode_select and
+// msa_dense_decode: `scores` null means `topk` is the input list; otherwise the
+// lists are selected from the strided scores inside the attend kernel and
+// written to `topk`.  dense_span > 0: no list, every visible block
+// (msa_dense_decode).  cu_q non-null: a prefill-style batch of T tokens,
+// request b owning tokens [cu_q[b], cu_q[b + 1]) (msa_sparse_prefill); Q is
+// then unused.  Nothing is enqueued; *empty is set when there is no work.
+int prepare_attend(const void* q, const void* kv, const int32_t* block_table,
+                   const int32_t* seq_lens, const float* scores, int64_t stride_h,
+                   int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
+                   size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                   int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                   int num_splits, int dense_span, float q_scale, const int32_t* cu_q, int T,
+                   AttendLaunch* L, bool* empty) {
+  *empty = true;
   if (!(q_scale == 0.f || finite_pos(q_scale))) return MSA_EINVAL;
   if (cu_q) {
     // the token count takes the place of B * Q in every size below
@@ -307,10 +336,10 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   const size_t need = msa_workspace_bytes(tb, tq, Hq, splits);
   if (splits > 1 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
     return MSA_ENOSPC;
-  CUtensorMap map;
-  if ((st = encode_kv_map(kv, Hkv, num_blocks, &map)) != MSA_OK) return st;
+  if ((st = encode_kv_map(kv, Hkv, num_blocks, &L->map)) != MSA_OK) return st;
   const int64_t rows = static_cast<int64_t>(tb) * tq * Hq;
-  msa::AttendParams p{};
+  msa::AttendParams& p = L->p;
+  p = msa::AttendParams{};
   p.q = q_scale > 0.f ? nullptr : static_cast<const uint16_t*>(q);
   p.q8 = q_scale > 0.f ? static_cast<const uint8_t*>(q) : nullptr;
   p.q_scale = q_scale;
@@ -338,12 +367,37 @@ int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
   p.v_scale = v_scale;
   p.cu_q = cu_q;
   p.T = cu_q ? T : 0;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = from_cuda(msa::launch_attend(map, p, s))) != MSA_OK) return st;
-  if (splits > 1)
-    return from_cuda(
-        msa::launch_combine(p.part_o, p.part_ml, static_cast<uint16_t*>(out), rows, splits, s));
+  L->rows = rows;
+  *empty = false;
   return MSA_OK;
+}
+
+// Enqueues a prepared attend (+ the split merge); `pdl` for the attend kernel
+// (the merge always follows it with programmatic serialization).
+int enqueue_attend(const AttendLaunch& L, cudaStream_t s, bool pdl) {
+  int st;
+  if ((st = from_cuda(msa::launch_attend(L.map, L.p, s, pdl))) != MSA_OK) return st;
+  if (L.p.splits > 1)
+    return from_cuda(
+        msa::launch_combine(L.p.part_o, L.p.part_ml, L.p.out, L.rows, L.p.splits, s, true));
+  return MSA_OK;
+}
+
+int sparse_decode(const void* q, const void* kv, const int32_t* block_table,
+                  const int32_t* seq_lens, const float* scores, int64_t stride_h,
+                  int64_t stride_t, int64_t stride_n, int32_t* topk, void* workspace,
+                  size_t workspace_bytes, void* out, int B, int Q, int Hq, int Hkv, int S,
+                  int64_t num_blocks, float sm_scale, float k_scale, float v_scale,
+                  int num_splits, msa_stream_t stream, int dense_span = 0, float q_scale = 0.f,
+                  const int32_t* cu_q = nullptr, int T = 0) {
+  AttendLaunch L;
+  bool empty;
+  const int st = prepare_attend(q, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n,
+                                topk, workspace, workspace_bytes, out, B, Q, Hq, Hkv, S,
+                                num_blocks, sm_scale, k_scale, v_scale, num_splits, dense_span,
+                                q_scale, cu_q, T, &L, &empty);
+  if (st != MSA_OK || empty) return st;
+  return enqueue_attend(L, reinterpret_cast<cudaStream_t>(stream), input_overlap());
 }
 
 }  // namespace
@@ -481,6 +535,61 @@ int msa_sparse_prefill_select_q8(const void* q8, float q_scale, const void* kv,
   return sparse_decode(q8, kv, block_table, seq_lens, scores, stride_h, stride_t, stride_n, topk,
                        workspace, workspace_bytes, out, B, 1, Hq, Hkv, S, num_blocks, sm_scale,
                        k_scale, v_scale, num_splits, stream, 0, q_scale, cu_seqlens_q, T);
+}
+
+// One decode step: the scorer, then the selection and the attend.  Rows of at
+// most kFusedMaxBlocks candidate blocks are selected inside the attend kernel
+// (msa_sparse_decode_select); longer rows by the selector kernel, whose
+// register paths hold up to 2048 candidates, then msa_sparse_decode.  The
+// first kernel follows the input-overlap setting; the others follow a library
+// kernel and may overlap it.
+int msa_decode_step(const void* q, float q_scale, const void* kv, const void* index_k,
+                    float index_k_scale, const int32_t* block_table, const int32_t* seq_lens,
+                    float* scores, int32_t* topk, void* workspace, size_t workspace_bytes,
+                    void* out, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
+                    float sm_scale, float k_scale, float v_scale, int num_splits,
+                    msa_stream_t stream) {
+  constexpr int kFusedMaxBlocks = 512;
+  if (!(q_scale == 0.f || finite_pos(q_scale))) return MSA_EINVAL;
+  if (index_k && !finite_pos(index_k_scale)) return MSA_EINVAL;
+  if (static_cast<int64_t>(B) * Q * Hkv > INT_MAX / 2) return MSA_EINVAL;
+  msa::ScoreParams sp;
+  CUtensorMap smap;
+  int st = prepare_score(q, q_scale, index_k ? index_k : kv, block_table, seq_lens, scores, B, Q,
+                         Hq, Hkv, S, num_blocks, sm_scale, index_k ? index_k_scale : k_scale,
+                         index_k != nullptr, &sp, &smap);
+  if (st != MSA_OK) return st;
+  const bool fused = S <= kFusedMaxBlocks;
+  const int64_t T = static_cast<int64_t>(B) * Q;
+  AttendLaunch L;
+  bool empty;
+  // the scores buffer [Hkv, T, S], block dim contiguous
+  st = prepare_attend(q, kv, block_table, seq_lens, fused ? scores : nullptr, T * S, S, 1, topk,
+                      workspace, workspace_bytes, out, B, Q, Hq, Hkv, S, num_blocks, sm_scale,
+                      k_scale, v_scale, num_splits, 0, q_scale, nullptr, 0, &L, &empty);
+  if (st != MSA_OK || empty || B == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = from_cuda(msa::launch_score(smap, sp, s, input_overlap()))) != MSA_OK) return st;
+  if (!fused) {
+    msa::TopkParams tp{};
+    tp.scores = scores;
+    tp.stride_h = T * S;
+    tp.stride_t = S;
+    tp.stride_n = 1;
+    tp.seq_lens = seq_lens;
+    tp.topk = topk;
+    tp.err = sp.err;
+    tp.B = B;
+    tp.Q = Q;
+    tp.Hkv = Hkv;
+    tp.S = S;
+    if ((st = from_cuda(msa::launch_topk(tp, s, true))) != MSA_OK) return st;
+  }
+  return enqueue_attend(L, s, true);
+}
+
+int msa_set_input_overlap(int enable) {
+  return g_input_overlap.exchange(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 int msa_get_error(unsigned int* flags, int clear) {

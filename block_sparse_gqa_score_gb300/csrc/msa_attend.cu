@@ -678,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // Split merge: one warp per (token, query head) row, 4 d-values per lane.
+// A part counts only when its l > 0 and its m is a number.
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                    uint16_t* __restrict__ out, int64_t rows, int splits) {
@@ -689,7 +690,7 @@ __global__ void __launch_bounds__(256)
   float M = -INFINITY;
   for (int s = lane; s < splits; s += 32) {
     const float m = part_ml[(s * rows + r) * 2], l = part_ml[(s * rows + r) * 2 + 1];
-    if (l > 0.f) M = fmaxf(M, m);
+    if (l > 0.f && m == m) M = fmaxf(M, m);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(256)
   float den = 0.f;
   for (int s = 0; s < splits; ++s) {
     const float m = part_ml[(s * rows + r) * 2], l = part_ml[(s * rows + r) * 2 + 1];
-    if (!(l > 0.f)) continue;
+    if (!(l > 0.f) || m != m) continue;  // an empty part, or one with no valid maximum
     const float w = ex2(m - M);
     den += w * l;
     const float4 v = *reinterpret_cast<const float4*>(part_o + (s * rows + r) * kHeadDim + 4 * lane);
@@ -715,7 +716,8 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream) {
+cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream,
+                          bool pdl) {
   static_assert(kSmemBytes <= 227 * 1024, "attend shared memory");
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
@@ -737,25 +739,25 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   dim3 grid(T, p.Hkv, p.splits);
   const dim3 block(kThreads);
   if (p.cu_q)  // prefill-style batches take lists only (no dense mode)
-    return p.q8 ? launch_pdl(attend_kernel<false, true, true>, grid, block, kSmemBytes, stream,
+    return p.q8 ? launch_pdl(attend_kernel<false, true, true>, grid, block, kSmemBytes, stream, pdl,
                              kv_map, p)
-                : launch_pdl(attend_kernel<false, false, true>, grid, block, kSmemBytes, stream,
+                : launch_pdl(attend_kernel<false, false, true>, grid, block, kSmemBytes, stream, pdl,
                              kv_map, p);
   if (p.q8)
     return p.dense_span > 0
-               ? launch_pdl(attend_kernel<true, true>, grid, block, kSmemBytes, stream, kv_map, p)
-               : launch_pdl(attend_kernel<false, true>, grid, block, kSmemBytes, stream, kv_map, p);
+               ? launch_pdl(attend_kernel<true, true>, grid, block, kSmemBytes, stream, pdl, kv_map, p)
+               : launch_pdl(attend_kernel<false, true>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
   return p.dense_span > 0
-             ? launch_pdl(attend_kernel<true, false>, grid, block, kSmemBytes, stream, kv_map, p)
-             : launch_pdl(attend_kernel<false, false>, grid, block, kSmemBytes, stream, kv_map, p);
+             ? launch_pdl(attend_kernel<true, false>, grid, block, kSmemBytes, stream, pdl, kv_map, p)
+             : launch_pdl(attend_kernel<false, false>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
-                           int splits, cudaStream_t stream) {
+                           int splits, cudaStream_t stream, bool pdl) {
   const int64_t threads = rows * 32;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
-  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(block), 0, stream,
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(block), 0, stream, pdl,
                     part_o, part_ml, out, rows, splits);
 }
 

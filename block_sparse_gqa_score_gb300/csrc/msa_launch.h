@@ -79,12 +79,15 @@ inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& se
   return e;
 }
 
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous kernel on the stream finishes (its CTAs call pdl_wait before
-// touching that kernel's results).
+// Launch with programmatic stream serialization when `pdl` is set: the kernel
+// may then start while the previous kernel on the stream finishes (its CTAs
+// call pdl_wait before touching that kernel's results, but may read the
+// caller's inputs before it).  Without `pdl` it is an ordinary launch that
+// starts after all earlier work on the stream has completed (pdl_wait then
+// returns at once).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t stream, Args&&... args) {
+                              cudaStream_t stream, bool pdl, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -94,14 +97,20 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
-cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream);
+// Each launcher's `pdl`: whether its kernel may overlap the previous kernel on
+// the stream (see launch_pdl).  The first kernel of a public entry point
+// passes the library-wide input-overlap setting; a kernel that follows
+// another library kernel inside one call passes true.
+cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream,
+                         bool pdl);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream,
+                          bool pdl);
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
-                           int splits, cudaStream_t stream);
+                           int splits, cudaStream_t stream, bool pdl);
 
 }  // namespace msa

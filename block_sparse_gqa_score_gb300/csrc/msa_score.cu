@@ -581,7 +581,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
 
 }  // namespace
 
-cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream) {
+cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream,
+                         bool pdl) {
   if (p.ctas < 1) return cudaErrorInvalidValue;
   const ScoreGeometry G = score_geometry(p.Q);
   if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
@@ -603,10 +604,10 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   if (e != cudaSuccess) return e;
   const dim3 grid(p.ctas * G.per_sm), block(G.threads);
   if (G.nsub > 1)   // the wide instantiation (kWide) is the one built for G.threads
-    return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, kv_map, p)
-                : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, kv_map, p);
-  return p.q8 ? launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, kv_map, p)
-              : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, kv_map, p);
+    return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, pdl, kv_map, p)
+                : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, pdl, kv_map, p);
+  return p.q8 ? launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, pdl, kv_map, p)
+              : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, pdl, kv_map, p);
 }
 
 }  // namespace msa

@@ -49,10 +49,10 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const TopkParams p) {
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hkv;
   const int64_t grid = (rows + kWarps - 1) / kWarps;
-  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kWarps * 32), 0, stream,
+  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kWarps * 32), 0, stream, pdl,
                     p);
 }
 

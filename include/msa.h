@@ -16,6 +16,7 @@
  *                      batches: one query length per request (cu_seqlens_q)
  *   msa_score_kcache   stage 1 on a separate K-only (index-K) cache
  *   msa_*_q8           the same with an fp8 query and a per-tensor q_scale
+ *   msa_decode_step    stages 1-4 of one step in one call
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -25,6 +26,14 @@
  *  - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns without waiting.  No call
  *    synchronises the host except msa_get_error.
+ *  - Stream order: by default each call's work starts only after all work
+ *    enqueued earlier on `stream` has completed, so its inputs may be written
+ *    by any kernel or copy just before it.  Inside one call (and inside
+ *    msa_decode_step) a library kernel may start while the library kernel
+ *    before it finishes (programmatic dependent launch); it reads that
+ *    kernel's outputs only after it has completed.  msa_set_input_overlap
+ *    lets the first kernel of every call overlap the previous kernel too
+ *    (see there).
  *  - Sizes: B requests, Q = decode_query_len query tokens per request,
  *    T = B*Q query tokens ordered request-major (token i = b*Q + j; the
  *    prefill entry points take T and cu_seqlens_q instead of Q),
@@ -395,6 +404,52 @@ int msa_sparse_decode_static(const void *q, const void *kv, const int32_t *block
                              const int32_t *seq_lens, const int32_t *topk, void *out, int B,
                              int Q, int Hq, int Hkv, int S, int64_t num_blocks, float sm_scale,
                              float k_scale, float v_scale, int num_splits, msa_stream_t stream);
+
+/*
+ * msa_decode_step -- one whole decode step in one call: msa_score (or
+ * msa_score_kcache on `index_k`), then the block selection and the attend,
+ * as the TensorRT-LLM PR #17171 decode path chains its scorer, selector and
+ * flash-decoding kernels on one stream.
+ *   q_scale       0: q is bf16 [T, Hq, 128]; > 0: q is fp8 e4m3 whose value
+ *                 is q * q_scale (as the _q8 entry points)
+ *   index_k       NULL: the blocks are scored on kv's K halves with k_scale;
+ *                 else on this K-only cache [num_blocks, Hkv, 128, 128]
+ *                 (msa_score_kcache) with index_k_scale (finite, > 0)
+ *   scores        fp32 [Hkv, T, S], written (msa_score's output)
+ *   topk          int32 [T, Hkv, 16], written (msa_topk's output)
+ *   workspace     as msa_sparse_decode (msa_workspace_bytes(B, Q, Hq, s)
+ *                 bytes for the effective split count s > 1)
+ *   out           bf16 [T, Hq, 128]
+ * The result equals msa_score, msa_topk and msa_sparse_decode called in turn
+ * on the same arguments.  Rows of at most 512 candidate blocks (S <= 512) are
+ * selected inside the attend kernel (msa_sparse_decode_select), longer ones
+ * by the selector kernel.  Every argument is checked before anything is
+ * enqueued.  Errors: those of msa_score, msa_topk and msa_sparse_decode, plus
+ * q_scale < 0 or not finite, or index_k given with a bad index_k_scale
+ * (MSA_EINVAL).
+ */
+int msa_decode_step(const void *q, float q_scale, const void *kv, const void *index_k,
+                    float index_k_scale, const int32_t *block_table, const int32_t *seq_lens,
+                    float *scores, int32_t *topk, void *workspace, size_t workspace_bytes,
+                    void *out, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
+                    float sm_scale, float k_scale, float v_scale, int num_splits,
+                    msa_stream_t stream);
+
+/*
+ * msa_set_input_overlap -- whether the first kernel of each call may start
+ * before the previous kernel on its stream has finished (programmatic
+ * dependent launch), reading the call's inputs (q, kv, block_table, seq_lens,
+ * a given topk, cu_seqlens_q, a merge workspace) early, to overlap that
+ * kernel's tail.  Off (0) by default: each call then waits for all earlier
+ * work on its stream, and its inputs may be written by any kernel just
+ * before it.  Turn it on (non-zero) only when the kernel just before every
+ * call on the stream is one of this library's, or one that writes none of
+ * that call's inputs: a kernel that wrote them could otherwise be read
+ * before its writes are visible.  Outputs are always ordered: no library
+ * kernel writes a buffer before the previous kernel has finished.
+ * Process-wide; returns the previous setting (0 or 1).
+ */
+int msa_set_input_overlap(int enable);
 
 /*
  * Read the current device's sticky error word (an OR of MSA_ERR_* bits set by

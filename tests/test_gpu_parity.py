@@ -159,9 +159,15 @@ def test_combine_matches_oracle():
     l[:, 9] = 0.0                           # a row with every part empty
     m[:, 9] = -float("inf")
     ml = torch.stack([m, l], dim=-1)
-    ws = torch.cat([o.float().reshape(-1), ml.float().reshape(-1)]).to(DEV)
+    # a part whose maximum is NaN (l > 0) carries no softmax state: the merge
+    # skips it, i.e. its row equals the merge with that part marked empty
+    ml_nan = ml.clone()
+    ml_nan[2, 11, 0] = float("nan")
+    ml_ref = ml.clone()
+    ml_ref[2, 11, 1] = 0.0
+    ws = torch.cat([o.float().reshape(-1), ml_nan.float().reshape(-1)]).to(DEV)
     got = msa.combine(ws, T, Hq, splits)
-    want = oracle.combine(o.float().double().numpy(), ml.float().double().numpy())
+    want = oracle.combine(o.float().double().numpy(), ml_ref.float().double().numpy())
     g = _np(got).reshape(rows, 128)
     # the merged rows are rounded to bf16 (8 significant bits): half an ulp is
     # 2^-9 relative; allow 2^-8 relative plus fp32 noise

@@ -2,10 +2,13 @@
 only hold the step's inputs and outputs and cannot allocate device memory (no
 workspace from their host interface, no cudaMalloc on their hot path).
 
-It is checked through the C ABI against msa_sparse_decode on the same inputs,
-on two calls in a row (the scratch array keeps the previous call's contents,
-which must not leak into the next result).  This file sorts last so that a
-run stopping at its first failure has already run every other test."""
+It is checked through the C ABI against msa_sparse_decode (same kernels, same
+split count: the bits must be identical) and against the oracle, on calls in a
+row that alternate two different inputs of one shape (A, B, A): the scratch
+array keeps the previous call's partials, which must not leak into the next
+result.  A warmed-up call must leave the device's free memory unchanged.  This
+file sorts last so that a run stopping at its first failure has already run
+every other test."""
 from __future__ import annotations
 
 import ctypes
@@ -57,6 +60,14 @@ def _close(a: torch.Tensor, b: torch.Tensor):
     assert d.max().item() <= OUT_MAX_ABS and d.mean().item() <= OUT_MEAN_ABS
 
 
+def _oracle_close(got: torch.Tensor, inp, topk):
+    import oracle
+    from tests.helpers import assert_out_close, padding_rows, to_problem
+    ref = oracle.attend(to_problem(inp, oracle), topk.cpu().numpy())
+    assert_out_close(got.float().cpu().numpy().astype(np.float64), ref,
+                     padding_rows(inp.seq_lens_list, inp.qlen))
+
+
 CASES = [
     # seq_lens, qlen, Hq, Hkv, splits (0 = library's choice)
     ([2048, 3000], 1, 16, 1, 0),
@@ -64,21 +75,50 @@ CASES = [
 ]
 
 
-def test_static_scratch_matches_workspace_path_on_two_calls_in_a_row():
+def _splits(lib, inp, splits):
+    return splits or lib.msa_choose_splits(
+        inp.batch, inp.qlen, inp.num_kv_heads,
+        torch.cuda.get_device_properties(0).multi_processor_count)
+
+
+def test_static_scratch_matches_workspace_path_on_alternating_inputs():
     lib = _lib()
     for seq_lens, Q, Hq, Hkv, splits in CASES:
-        inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=211, device=DEV, kv_std=0.5,
-                             kv_scale_mode="amax")
-        topk = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(3)).to(DEV)
-        want = torch.empty_like(inp.q)
-        assert _call_with_workspace(lib, inp, topk, want, splits or
-                                    lib.msa_choose_splits(inp.batch, Q, Hkv,
-                                    torch.cuda.get_device_properties(0).multi_processor_count)) == 0
-        for _ in range(2):
+        # two inputs of one shape: different queries, caches and lists
+        inputs = []
+        for seed in (211, 212):
+            inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=seed, device=DEV, kv_std=0.5,
+                                 kv_scale_mode="amax")
+            topk = wl.draw_topk_given(seq_lens, Q, Hkv,
+                                      torch.Generator().manual_seed(seed)).to(DEV)
+            want = torch.empty_like(inp.q)
+            assert _call_with_workspace(lib, inp, topk, want, _splits(lib, inp, splits)) == 0
+            _oracle_close(want, inp, topk)
+            inputs.append((inp, topk, want))
+        assert not torch.equal(inputs[0][2], inputs[1][2])
+        for k in (0, 1, 0):
+            inp, topk, want = inputs[k]
             got = torch.full_like(inp.q, float("nan"))
             assert _call_static(lib, inp, topk, got, splits) == 0
             torch.cuda.synchronize()
+            assert torch.equal(got, want), "differs from msa_sparse_decode with the same splits"
             _close(got, want)
+
+
+def test_static_scratch_allocates_nothing():
+    lib = _lib()
+    seq_lens, Q, Hq, Hkv, splits = CASES[1]
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=213, device=DEV)
+    topk = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(4)).to(DEV)
+    out = torch.empty_like(inp.q)
+    assert _call_static(lib, inp, topk, out, splits) == 0      # warm-up: address look-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert _call_static(lib, inp, topk, out, splits) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size():
