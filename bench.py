@@ -69,6 +69,10 @@ def _args():
                     help="skip the end-to-end measurement (host copies, public API)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle beside the line")
+    ap.add_argument("--input-overlap", action="store_true",
+                    help="msa_set_input_overlap(1) for the timed steps: each step's first kernel "
+                         "may start while the previous step's last kernel finishes (valid here: "
+                         "that kernel writes none of the step's inputs); default off")
     ap.add_argument("--graph-chunk", type=int, default=250,
                     help="steps captured per CUDA graph in the timed region")
     return ap.parse_args()
@@ -452,6 +456,7 @@ def run_ours(args, rank, world, local):
 
     msa_build.build()
     msa._native.load()
+    msa.set_input_overlap(args.input_overlap)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.workload or wl.HEADLINE
@@ -467,7 +472,7 @@ def run_ours(args, rank, world, local):
     layers = [first] + [wl.make_inputs(w, device=dev, layer=l) for l in range(1, n_layers)]
     T = first.tokens   # every layer has the same request and query lengths
     # buffers and splits sized by tokens: B requests of qlen, or T prefill tokens
-    tb, tq = (1, T) if w.prefill_q else (w.batch, w.qlen)
+    tb, tq = (T, 1) if w.prefill_q else (w.batch, w.qlen)
     splits = msa.choose_splits(tb, tq, w.num_kv_heads, props.multi_processor_count)
     if w.dense:   # the split count of dense decode follows the block table's stride
         splits = max(msa.dense_splits(inp.stride) for inp in layers)
@@ -518,6 +523,17 @@ def run_ours(args, rank, world, local):
                                           out=bf.out, num_splits=bf.num_splits,
                                           workspace=bf.workspace, q_scale=inp.q_scale)]
 
+    def step_call(l):
+        """One whole step through the public API: msa_decode_step (score, then
+        selection and attend in one library call), or the attend alone."""
+        inp, bf = layers[l], bufs[l]
+        if attend_only:
+            stage_calls(l)[2]()
+            return
+        msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen, inp.sm_scale,
+                        inp.k_scale, inp.v_scale, buffers=bf, q_scale=inp.q_scale,
+                        index_k=inp.index_k, index_k_scale=inp.index_k_scale)
+
     attend_only = w.topk_given or w.dense
     fused = (not attend_only) and msa.fused_selection(first.stride)
     launches_per_step = (1 if attend_only else (2 if fused else 3)) + (1 if splits > 1 else 0)
@@ -526,8 +542,7 @@ def run_ours(args, rank, world, local):
     msa.get_error(clear=True)
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
-            for f in stage_calls(k % n_layers):
-                f()
+            step_call(k % n_layers)
     torch.cuda.synchronize(dev)
     flags = msa.get_error(clear=True)
     works = []
@@ -541,13 +556,22 @@ def run_ours(args, rank, world, local):
     graphs = []
     mode = "cuda-graph"
 
-    def capture(nsteps, which=(0, 1, 2)):
+    def capture(nsteps, which=None):
+        """A graph of `nsteps` whole steps, or of one stage's launches alone
+        (`which`: its index in stage_calls), replayed as a chain of library
+        calls with the input overlap on (each launch follows another of the
+        same kernel, which writes none of its inputs)."""
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(nsteps):
-                calls = stage_calls(k % n_layers)
-                for s_i in which:
-                    calls[s_i]()
+        prev = msa.set_input_overlap(which is not None or args.input_overlap)
+        try:
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(nsteps):
+                    if which is None:
+                        step_call(k % n_layers)
+                    else:
+                        stage_calls(k % n_layers)[which]()
+        finally:
+            msa.set_input_overlap(prev)
         return g
 
     try:
@@ -578,8 +602,7 @@ def run_ours(args, rank, world, local):
                     g.replay()
         else:
             for k in range(args.steps):
-                for f in stage_calls(k % n_layers):
-                    f()
+                step_call(k % n_layers)
     stop.record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark_stop()
@@ -600,7 +623,7 @@ def run_ours(args, rank, world, local):
         if (k == "topk" and fused) or (attend_only and k != "attend"):
             continue   # fused: the selection is part of the attend kernel
         try:
-            g = capture(reps_stage, which=(s_i,)) if graphs else None
+            g = capture(reps_stage, which=s_i) if graphs else None
         except Exception:  # pragma: no cover
             g = None
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -630,9 +653,13 @@ def run_ours(args, rank, world, local):
         g = None
         if graphs:
             g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for j in range(reps_stage):
-                    plain(j % n_layers)
+            prev = msa.set_input_overlap(True)    # a chain of attend launches, as above
+            try:
+                with torch.cuda.graph(g, stream=stream):
+                    for j in range(reps_stage):
+                        plain(j % n_layers)
+            finally:
+                msa.set_input_overlap(prev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             if g is not None:
@@ -708,7 +735,8 @@ def run_ours(args, rank, world, local):
             "config": dict(w.describe(), layers_rotated=n_layers,
                            l2_policy=f"inputs larger than L2: {n_layers} independent layers "
                                      f"({layer_bytes * n_layers / 1e9:.2f} GB) rotated",
-                           splits=splits, timing=mode, parallelism=f"replicas x{world}"),
+                           splits=splits, timing=mode, parallelism=f"replicas x{world}",
+                           input_overlap=bool(args.input_overlap)),
             "roofline": roofline, "stages": stages, "attend_gathered_kv": gathered,
             "stage_sum_vs_step": sum(avg_ms.values()) / (total_ms / args.steps),
             "gpu_launches": launches_per_step * args.steps, "error_flags": flags}

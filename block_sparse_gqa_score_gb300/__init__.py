@@ -41,7 +41,8 @@ __all__ = ["score", "topk", "sparse_decode", "sparse_decode_select", "sparse_pre
            "sparse_prefill_select", "dense_decode", "dense_splits",
            "combine", "decode_step",
            "fused_selection", "FUSED_MAX_BLOCKS", "workspace_bytes",
-           "choose_splits", "get_error", "set_input_overlap", "DecodeBuffers", "MSAError"]
+           "choose_splits", "get_error", "set_input_overlap", "set_union_tile", "DecodeBuffers",
+           "MSAError"]
 
 
 def _lib():
@@ -289,8 +290,9 @@ def _prefill_geometry(q, kv, block_table, seq_lens, cu_seqlens_q):
 
 
 def _prefill_splits(T: int, Hq: int, Hkv: int, num_splits: int, workspace, dev):
-    splits = num_splits if num_splits > 0 else choose_splits(1, max(T, 1), Hkv)
-    need = workspace_bytes(1, max(T, 1), Hq, splits)
+    # one CTA per token: the single-token rule, choose_splits(T, 1, ...)
+    splits = num_splits if num_splits > 0 else choose_splits(max(T, 1), 1, Hkv)
+    need = workspace_bytes(max(T, 1), 1, Hq, splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
@@ -438,6 +440,15 @@ def decode_step(q, kv, block_table, seq_lens, qlen: int, sm_scale: float, k_scal
         float(k_scale), float(v_scale), bf.num_splits, _stream(dev, stream))
     _native.check(st, "msa_decode_step")
     return bf.scores, bf.topk, bf.out
+
+
+def set_union_tile(enable: bool) -> bool:
+    """msa_set_union_tile: attend sparse decode steps of two or more tokens per
+    request over the union of each 4-token tile's lists, loading each shared
+    page once (pays off when a request's tokens list mostly the same blocks).
+    Off by default; dense decode always works this way.  Returns the previous
+    setting."""
+    return bool(_lib().msa_set_union_tile(1 if enable else 0))
 
 
 def set_input_overlap(enable: bool) -> bool:

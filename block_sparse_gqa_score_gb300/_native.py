@@ -25,7 +25,7 @@ EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode_select_q8", "msa_dense_decode_q8", "msa_sparse_prefill",
            "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
            "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
-           "msa_set_input_overlap")
+           "msa_set_input_overlap", "msa_set_union_tile")
 
 _lib = None
 _lock = threading.Lock()
@@ -92,6 +92,7 @@ def load(path: str | None = None):
         lib.msa_decode_step.argtypes = [P, f32, P, P, f32, P, P, P, P, P, sz, P, i32, i32, i32,
                                         i32, i32, i64, f32, f32, f32, i32, P]
         lib.msa_set_input_overlap.argtypes = [i32]
+        lib.msa_set_union_tile.argtypes = [i32]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
@@ -102,7 +103,7 @@ def load(path: str | None = None):
                      "msa_dense_decode_q8", "msa_sparse_prefill", "msa_sparse_prefill_select",
                      "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
                      "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
-                     "msa_set_input_overlap"):
+                     "msa_set_input_overlap", "msa_set_union_tile"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -33,6 +33,9 @@ DeviceState g_dev[kMaxDevices];
 // msa_set_input_overlap: whether each entry point's first kernel may start
 // before the previous kernel on its stream has finished (off by default)
 std::atomic<int> g_input_overlap{0};
+// msa_set_union_tile: sparse decode steps of Q >= 2 over the union of each
+// 4-token tile's lists (off by default; dense decode always shares pages)
+std::atomic<int> g_union_tile{0};
 
 bool input_overlap() { return g_input_overlap.load(std::memory_order_relaxed) != 0; }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -137,6 +140,11 @@ size_t msa_workspace_bytes(int B, int Q, int Hq, int num_splits) {
 
 int msa_choose_splits(int B, int Q, int Hkv, int sm_count) {
   if (B < 1 || Q < 1 || Hkv < 1 || sm_count < 1) return 1;
+  if (Q >= 2 && g_union_tile.load(std::memory_order_relaxed)) {
+    // the union attend: one CTA per SM per (request, 4-token tile, KV head)
+    const int64_t units = static_cast<int64_t>(B) * ((Q + msa::kUnionTile - 1) / msa::kUnionTile) * Hkv;
+    return msa::union_ctas_per_unit(units > INT_MAX ? INT_MAX : static_cast<int>(units), sm_count);
+  }
   const int64_t units = static_cast<int64_t>(B) * Q * Hkv;  // one CTA per (token, KV head)
   const int64_t slots = 2 * static_cast<int64_t>(sm_count);  // two CTAs per SM
   if (units * 4 >= slots * 3) return 1;
@@ -332,7 +340,22 @@ int prepare_attend(const void* q, const void* kv, const int32_t* block_table,
   if ((st = device_state(&dev)) != MSA_OK) return st;
   // sizes over tokens: B requests of Q, or T tokens of a prefill-style batch
   const int tb = cu_q ? 1 : B, tq = cu_q ? T : Q;
-  const int splits = num_splits == 0 ? msa_choose_splits(tb, tq, Hkv, dev->sm_count) : num_splits;
+  // the union attend: dense decode, or sparse decode when the union mode is on,
+  // with two or more tokens per request
+  const bool union_tile = !cu_q && Q >= 2 &&
+                          (dense_span > 0 || g_union_tile.load(std::memory_order_relaxed) != 0);
+  // prefill batches (one CTA per token): the single-token rule, msa_choose_splits(T, 1, ...)
+  int splits = num_splits != 0 ? num_splits
+               : cu_q ? msa_choose_splits(T, 1, Hkv, dev->sm_count)
+                      : msa_choose_splits(B, Q, Hkv, dev->sm_count);
+  if (union_tile && dense_span > 0) {
+    // dense decode over the union: at most the caller's split count (which
+    // sized the workspace), at most one CTA per SM
+    const int64_t units = static_cast<int64_t>(B) * ((Q + msa::kUnionTile - 1) / msa::kUnionTile) * Hkv;
+    const int z = msa::union_ctas_per_unit(units > INT_MAX ? INT_MAX : static_cast<int>(units),
+                                           dev->sm_count);
+    splits = splits < z ? splits : z;
+  }
   const size_t need = msa_workspace_bytes(tb, tq, Hq, splits);
   if (splits > 1 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
     return MSA_ENOSPC;
@@ -367,6 +390,7 @@ int prepare_attend(const void* q, const void* kv, const int32_t* block_table,
   p.v_scale = v_scale;
   p.cu_q = cu_q;
   p.T = cu_q ? T : 0;
+  p.union_tile = union_tile ? 1 : 0;
   L->rows = rows;
   *empty = false;
   return MSA_OK;
@@ -586,6 +610,10 @@ int msa_decode_step(const void* q, float q_scale, const void* kv, const void* in
     if ((st = from_cuda(msa::launch_topk(tp, s, true))) != MSA_OK) return st;
   }
   return enqueue_attend(L, s, true);
+}
+
+int msa_set_union_tile(int enable) {
+  return g_union_tile.exchange(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 int msa_set_input_overlap(int enable) {

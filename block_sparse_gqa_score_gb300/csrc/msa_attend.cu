@@ -735,6 +735,8 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
+  // the union attend: one pass over the pages a 4-token tile shares
+  if (p.union_tile) return launch_union_attend(kv_map, p, stream, pdl);
   const int T = p.cu_q ? p.T : p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
   const dim3 block(kThreads);

@@ -62,6 +62,9 @@ struct AttendParams {
   // T tokens (then Q is unused); nullptr: every request has Q tokens
   const int32_t* cu_q;
   int T;
+  // 1: the union attend (msa_union.cu) over 4-token tiles of each request;
+  // 0: one CTA per (token, KV head)
+  int union_tile;
 };
 
 // Runs `set_up` once per device (e.g. raising a kernel's dynamic shared-memory
@@ -110,6 +113,16 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cudaStream_t stream,
                           bool pdl);
+// The union attend (msa_union.cu): decode steps of Q >= 2 tokens per request,
+// one CTA per (request, tile of 4 tokens, KV head, split) over the union of the
+// tile's lists; grid (B * ceil(Q / 4) * Hkv, splits).
+cudaError_t launch_union_attend(const CUtensorMap& kv_map, const AttendParams& p,
+                                cudaStream_t stream, bool pdl);
+// Its split count for `units` (request, tile, KV head) units: as many CTAs per
+// unit as fit one CTA per SM (at most 8), 1 when the units fill the SMs.
+int union_ctas_per_unit(int units, int sm_count);
+constexpr int kUnionTile = 4;   // query tokens per union tile
+
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
                            int splits, cudaStream_t stream, bool pdl);
 

@@ -175,9 +175,13 @@ int msa_topk(const float *scores, int64_t stride_h, int64_t stride_t, int64_t st
 size_t msa_workspace_bytes(int B, int Q, int Hq, int num_splits);
 
 /*
- * Split-K factor the library would pick for this shape on a GPU with
- * `sm_count` SMs.  Depends on the shape only (never on seq_lens), so a step
- * captured in a CUDA graph keeps a fixed launch shape.  Returns >= 1.
+ * Split-K factor the library would pick for a decode step of B requests of Q
+ * tokens on a GPU with `sm_count` SMs.  Q = 1: one CTA per (token, KV head),
+ * split while those fill less than three quarters of two CTAs per SM.  Q >= 2
+ * (the attend over the union of each 4-token tile's lists, one CTA per SM):
+ * min(8, sm_count / units) CTAs per (request, tile, KV head) unit, 1 when the
+ * units fill the SMs.  Depends on the shape only (never on seq_lens), so a
+ * step captured in a CUDA graph keeps a fixed launch shape.  Returns >= 1.
  */
 int msa_choose_splits(int B, int Q, int Hkv, int sm_count);
 
@@ -310,8 +314,8 @@ int msa_dense_decode_q8(const void *q8, float q_scale, const void *kv,
  * cu_seqlens_q: int32 [B + 1] on the device, cu_seqlens_q[0] = 0, ascending,
  * cu_seqlens_q[B] = T (read by the kernel only, so it may be written by an
  * earlier kernel on `stream`).  Workspace for num_splits > 1:
- * msa_workspace_bytes(1, T, Hq, splits); num_splits = 0 chooses
- * msa_choose_splits(1, T, Hkv, sm_count).
+ * msa_workspace_bytes(T, 1, Hq, splits); num_splits = 0 chooses
+ * msa_choose_splits(T, 1, Hkv, sm_count) (one CTA per token).
  * Errors: as msa_sparse_decode, plus null or misaligned cu_seqlens_q, T < 0
  * or T > INT_MAX / 4, or exactly one of B and T zero (MSA_EINVAL); no query
  * length bound applies.  Device: a token in no request's range (e.g. past
@@ -434,6 +438,24 @@ int msa_decode_step(const void *q, float q_scale, const void *kv, const void *in
                     void *out, int B, int Q, int Hq, int Hkv, int S, int64_t num_blocks,
                     float sm_scale, float k_scale, float v_scale, int num_splits,
                     msa_stream_t stream);
+
+/*
+ * msa_set_union_tile -- how msa_sparse_decode(_select) (and msa_decode_step,
+ * msa_sparse_decode_static) attend decode steps of Q >= 2 tokens per request.
+ * Off (0, the default): one CTA per (token, KV head), each loading its own
+ * token's listed pages.  On (non-zero): one CTA per (request, tile of 4
+ * consecutive tokens, KV head, split) over the union of the tile's lists,
+ * each union page loaded once and attended by the tokens that listed it (the
+ * way the vLLM CUTLASS decode plan sizes a request's work by its query
+ * length).  This pays off when a request's tokens list mostly the same
+ * blocks; with lists that overlap little (e.g. 52 distinct pages for 64
+ * listed ones) the one-CTA-per-token form is faster on a GB300.  Results
+ * agree within the output tolerance (the accumulation order differs).  The
+ * split count msa_choose_splits reports follows this setting.  Dense decode
+ * (msa_dense_decode) always attends a tile's shared pages this way when
+ * Q >= 2.  Process-wide; returns the previous setting (0 or 1).
+ */
+int msa_set_union_tile(int enable);
 
 /*
  * msa_set_input_overlap -- whether the first kernel of each call may start

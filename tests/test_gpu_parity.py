@@ -302,18 +302,28 @@ def test_dense_decode_matches_oracle(seq_lens, Q, Hq, Hkv):
     assert msa.get_error() == 0
 
 
-def test_dense_decode_equals_sparse_decode_on_short_rows():
+@pytest.mark.parametrize("Q", [1, 4])
+def test_dense_decode_equals_sparse_decode_on_short_rows(Q):
     """With at most 16 visible blocks per row, dense decode and the sparse
-    attend over all-visible lists take the same pages in the same order: the
-    same bits."""
-    seq_lens, Q, Hq, Hkv = [257, 513, 2048, 1, 0], 4, 64, 4
+    attend over all-visible lists attend the same keys.  With one token per
+    request both run one CTA per token over the same pages in the same order:
+    the same bits.  With several, the sparse attend shares each page between
+    the request's tokens (accumulating in another order): within the output
+    tolerance of each other and of the oracle."""
+    seq_lens, Hq, Hkv = [257, 513, 2048, 1, 0], 64, 4
     inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=111, device=DEV, kv_std=0.5)
     dense = msa.dense_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
                              inp.k_scale, inp.v_scale)
     topk = wl.all_visible_topk(seq_lens, Q, Hkv).to(DEV)
     sparse = msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, topk, Q,
                                inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=1)
-    assert torch.equal(dense, sparse)
+    if Q == 1:
+        assert torch.equal(dense, sparse)
+    else:
+        ref = oracle.attend(to_problem(inp, oracle), topk.cpu().numpy())
+        assert_out_close(_np(dense), ref, padding_rows(seq_lens, Q))
+        assert_out_close(_np(sparse), ref, padding_rows(seq_lens, Q))
+        assert_out_close(_np(sparse), _np(dense))
     assert msa.get_error() == 0
 
 
@@ -473,6 +483,9 @@ def test_prefill_fp8_query_all_visible_pages():
 
 @pytest.mark.parametrize("splits", [1, 2])
 def test_prefill_with_equal_lengths_is_bit_identical_to_decode(splits):
+    """Equal query lengths put prefill tokens at the decode positions, and both
+    entry points then run one CTA per token over the same pages (the default
+    decode attend): the same bits."""
     seq_lens, Q, Hq, Hkv = [20000, 9000, 300, 4100], 8, 64, 4
     inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=123, device=DEV, kv_std=0.5)
     topk = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(13)).to(DEV)
