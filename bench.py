@@ -73,6 +73,9 @@ def _args():
                     help="msa_set_input_overlap(1) for the timed steps: each step's first kernel "
                          "may start while the previous step's last kernel finishes (valid here: "
                          "that kernel writes none of the step's inputs); default off")
+    ap.add_argument("--union-tile", action="store_true",
+                    help="msa_set_union_tile(1): attend each request's 4-token tiles over the union "
+                         "of their lists (default: one CTA per token)")
     ap.add_argument("--graph-chunk", type=int, default=250,
                     help="steps captured per CUDA graph in the timed region")
     return ap.parse_args()
@@ -457,6 +460,7 @@ def run_ours(args, rank, world, local):
     msa_build.build()
     msa._native.load()
     msa.set_input_overlap(args.input_overlap)
+    msa.set_union_tile(args.union_tile)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.workload or wl.HEADLINE
@@ -736,7 +740,8 @@ def run_ours(args, rank, world, local):
                            l2_policy=f"inputs larger than L2: {n_layers} independent layers "
                                      f"({layer_bytes * n_layers / 1e9:.2f} GB) rotated",
                            splits=splits, timing=mode, parallelism=f"replicas x{world}",
-                           input_overlap=bool(args.input_overlap)),
+                           input_overlap=bool(args.input_overlap),
+                           union_tile=bool(args.union_tile)),
             "roofline": roofline, "stages": stages, "attend_gathered_kv": gathered,
             "stage_sum_vs_step": sum(avg_ms.values()) / (total_ms / args.steps),
             "gpu_launches": launches_per_step * args.steps, "error_flags": flags}

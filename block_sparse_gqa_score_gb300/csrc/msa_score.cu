@@ -59,6 +59,7 @@ struct ScoreTail {
   uint64_t qfull[2];           // query prep -> MMA (query tile ready)
   uint64_t qempty[2];          // MMA -> query prep (query tile no longer read)
   uint64_t qmul_ready[kQmulRing];  // query prep -> epilogue (unit scale factors)
+  uint64_t qstage;             // query prep -> TMA: the last stage, the first tile's staging, is free
   uint64_t finish;             // every role finished (TMEM may be freed)
   uint32_t tmem_base;
   int start_b, start_rem, count;   // this CTA's page range
@@ -87,13 +88,19 @@ __host__ __device__ inline ScoreGeometry score_geometry(int Q) {
   while (nc < cols) nc <<= 1;
   G.ncols = nc;
   G.qtile_bytes = 2 * 16 * Q * 128;
-  G.nqb = (2 * G.qtile_bytes <= 64 * 1024) ? 2 : 1;   // double-buffer small query tiles
-  const int fixed1 = G.nqb * G.qtile_bytes + align16(kQmulRing * Q * 4) +
-                     align16(kRedSlots * 4 * Q * 4) + align16(static_cast<int>(sizeof(ScoreTail))) +
-                     1024;
   // two CTAs per SM (two independent pipelines) when tensor memory and shared
   // memory hold two; each then gets half an SM's shared memory
   const int two_budget = kSmemPerSM / 2 - 1024;
+  // Small query tiles are double-buffered: the next unit's tile is built
+  // while the current one is in use.  (A single buffer, which leaves room for
+  // one more K stage at qlen 2-8, measured slower at qlen 4: 43.1 vs 40.3 us,
+  // the tile hand-over at a unit boundary stalling the CTAs that cross one.)
+  G.nqb = (2 * G.qtile_bytes <= 64 * 1024) ? 2 : 1;
+  auto fixed_for = [&](int nqb) {
+    return nqb * G.qtile_bytes + align16(kQmulRing * Q * 4) + align16(kRedSlots * 4 * Q * 4) +
+           align16(static_cast<int>(sizeof(ScoreTail))) + 1024;
+  };
+  const int fixed1 = fixed_for(G.nqb);
   G.per_sm = (nc <= 256 && (two_budget - fixed1) / kHalfTile >= 3) ? 2 : 1;
   // one CTA per SM has the registers for a second set of epilogue warps
   G.nsub = G.per_sm == 1 ? kWideSub : 1;
@@ -109,6 +116,12 @@ __host__ __device__ inline ScoreGeometry score_geometry(int Q) {
   G.off_tail = G.off_red + red_bytes;
   G.smem = G.off_tail + align16(static_cast<int>(sizeof(ScoreTail))) + 1024;
   return G;
+}
+
+// Whether the first query tile is staged through the last K stage: one
+// query buffer, and the tile's raw rows (Q tokens x 16 rows) fit in a stage.
+__host__ __device__ inline bool stage_staging(const ScoreGeometry& G, bool fp8) {
+  return G.nqb == 1 && G.Q * kGroup * (fp8 ? 128 : 256) <= kHalfTile;
 }
 
 __device__ __forceinline__ int order_int(float x) {
@@ -183,17 +196,53 @@ __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk&
 // Query tile of unit (b, g) into hi / lo (16 Q rows x 128 B each, 128B
 // swizzled, K-major), per-token factors into qmul[0..Q): a bf16 query scaled
 // by 2^-e and split exactly into hi + lo (factor scale * 2^e), or an fp8 query
-// as stored in hi (lo unused; factor scale * q_scale).
+// as stored in hi (lo unused; factor scale * q_scale).  With `staging` (at
+// least Q * 4 KiB of shared memory nothing else uses meanwhile), every token's
+// rows are first copied there with asynchronous copies, all in flight at
+// once, so the tile costs one memory round trip instead of one per token.
 template <bool kFp8Q>
 __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
-                                   float* qmul, int lane) {
+                                   float* qmul, int lane, uint8_t* staging) {
+  constexpr int kRowBytes = kFp8Q ? 128 : 256;   // one query head's row
+  constexpr int kTokBytes = kGroup * kRowBytes;  // one token's 16 rows, contiguous
+  if (staging) {
+    for (int jq = 0; jq < p.Q; ++jq) {
+      const int64_t row = (static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup;
+      const uint8_t* src = kFp8Q ? p.q8 + row * kHeadDim
+                                 : reinterpret_cast<const uint8_t*>(p.q + row * kHeadDim);
+      for (int c = lane; c < kTokBytes / 16; c += 32)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(
+                         smem_u32(staging + jq * kTokBytes + 16 * c)),
+                     "l"(src + 16 * c)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
   for (int jq = 0; jq < p.Q; ++jq) {
     const int64_t row = (static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup;
     if constexpr (kFp8Q) {
-      store_query_rows_fp8(p.q8 + row * kHeadDim, jq * kGroup, qhi, lane);
+      if (staging) {
+        // lane l: 64 bytes of row l / 2, copied as stored into the swizzled tile
+        const int r = lane >> 1, half = lane & 1;
+        const uint4* src = reinterpret_cast<const uint4*>(staging + jq * kTokBytes + r * 128 + 64 * half);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(qhi + sw128(jq * kGroup + r, 4 * half + k)) = src[k];
+      } else
+        store_query_rows_fp8(p.q8 + row * kHeadDim, jq * kGroup, qhi, lane);
       if (lane == 0) qmul[jq] = p.scale * p.q_scale;
     } else {
-      const int e = prepare_query_e4m3(p.q + row * kHeadDim, jq * kGroup, qhi, qlo, lane);
+      uint4 raw[8];
+      if (staging) {
+        const uint4* src = reinterpret_cast<const uint4*>(staging + jq * kTokBytes +
+                                                          (lane >> 1) * kRowBytes + 128 * (lane & 1));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) raw[k] = src[k];
+      } else {
+        load_query_rows(p.q + row * kHeadDim, lane, raw);
+      }
+      const int e = store_query_e4m3(raw, jq * kGroup, qhi, qlo, lane);
       if (lane == 0) qmul[jq] = p.scale * exp2i(e);
     }
   }
@@ -283,6 +332,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       mbar_init(&tail->red_empty[s], 1);
     }
     for (int s = 0; s < kQmulRing; ++s) mbar_init(&tail->qmul_ready[s], 1);
+    mbar_init(&tail->qstage, 1);
     mbar_init(&tail->finish, kNumThreads / 32);
     tail->any_invalid = 0;
     fence_barrier_init();
@@ -335,6 +385,11 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
         }
         const int s = vp % G.stages;
         if (vp >= G.stages && !mbar_wait(&tail->empty[s], ((vp / G.stages) - 1) & 1)) {
+          flag_error(p.err, MSA_ERR_TIMEOUT);
+          break;
+        }
+        // with one query buffer the last stage first stages the first query tile
+        if (stage_staging(G, kFp8Q) && vp == G.stages - 1 && !mbar_wait(&tail->qstage, 0)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
@@ -436,16 +491,36 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       }
       uint8_t* qhi = qtiles + qb * G.qtile_bytes;
       float* qmul = qmul_ring + (k % kQmulRing) * Q;
-      prepare_query_tile<kFp8Q>(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane);
-      tc::fence_proxy_async_smem();   // the tile is read by the tensor core
+      // the first tile, which the first products wait for, is staged through
+      // the second tile buffer (free until the second tile is built), or with
+      // a single buffer through the last K stage, which the producer loads
+      // only once this tile is built
+      uint8_t* staging = k != 0 ? nullptr
+                         : G.nqb == 2 ? qtiles + G.qtile_bytes
+                         : stage_staging(G, kFp8Q) ? stages + (G.stages - 1) * kHalfTile
+                                                   : nullptr;
+      prepare_query_tile<kFp8Q>(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane, staging);
+      tc::fence_proxy_async_smem();   // the tile is read by the tensor core (and the staging rewritten by TMA)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&tail->qfull[qb]);
         mbar_arrive(&tail->qmul_ready[k % kQmulRing]);
+        if (k == 0) mbar_arrive(&tail->qstage);
       }
       // skip to the first page of the next unit
       const int in_unit = w.nhi - w.n;
       for (int s = 0; s < in_unit && t < count; ++s, ++t) w.next(p);
+      // its query rows into L2 now, so that its tile is quick to build
+      if (t < count) {
+        constexpr int kTokBytes = kGroup * (kFp8Q ? 128 : 256);
+        for (int jq = 0; jq < Q; ++jq) {
+          const int64_t row = (static_cast<int64_t>(w.b) * Q + jq) * p.Hq + w.g * kGroup;
+          const uint8_t* src = kFp8Q ? p.q8 + row * kHeadDim
+                                     : reinterpret_cast<const uint8_t*>(p.q + row * kHeadDim);
+          for (int c = lane; c < kTokBytes / 128; c += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * c));
+        }
+      }
       ++k;
     }
     // -inf for blocks past each request's last visible block (units dealt

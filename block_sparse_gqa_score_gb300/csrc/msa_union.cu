@@ -296,9 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_proxy_async_smem();  // the tile is read by the tensor core
   }
-  tc::fence_before_thread_sync();
-  __syncthreads();
-  tc::fence_after_thread_sync();
+  // Warp 0 builds the union once the lists and the block-table row are in
+  // shared memory: a barrier over warps 0 and 3 and the list warps only, so
+  // that the query tiles are prepared meanwhile.
+  constexpr int kListBarrier = 1, kListThreads = 32 * (2 + kQt);
+  if (warp == 0 || warp == 3 || (warp >= kSoftWarp0 && (warp & 3) == 0))
+    named_barrier(kListBarrier, kListThreads);
 
   // ---- prologue, part 2 (warp 0): the union and this CTA's pages --------------------
   if (kDense && warp == 0) {
@@ -355,28 +358,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       v[r] = n >= 0 ? (static_cast<uint32_t>(n) << 2) | static_cast<uint32_t>(j) : 0xFFFFFFFFu;
     }
     warp_sort64(v, lane);
-    tail->sorted[lane] = v[0];
-    tail->sorted[32 + lane] = v[1];
-    __syncwarp();
+    // neighbours in sorted order by shuffles: the previous key, and the next
+    // four (a block's run is at most one key per token in a valid list)
+    uint32_t prev[2], nxt[2][4];
+    {
+      const uint32_t up0 = __shfl_up_sync(0xffffffffu, v[0], 1);
+      const uint32_t up1 = __shfl_up_sync(0xffffffffu, v[1], 1);
+      const uint32_t last0 = __shfl_sync(0xffffffffu, v[0], 31);
+      prev[0] = lane == 0 ? 0xFFFFFFFFu : up0;
+      prev[1] = lane == 0 ? last0 : up1;
+#pragma unroll
+      for (int d = 1; d <= 4; ++d) {
+        const uint32_t dn0 = __shfl_down_sync(0xffffffffu, v[0], d);
+        const uint32_t dn1 = __shfl_down_sync(0xffffffffu, v[1], d);
+        const uint32_t wrap = __shfl_sync(0xffffffffu, v[1], (lane + d) & 31);
+        nxt[0][d - 1] = lane + d < 32 ? dn0 : wrap;
+        nxt[1][d - 1] = lane + d < 32 ? dn1 : 0xFFFFFFFFu;
+      }
+    }
     // per distinct block: first occurrence, the tokens listing it, its page
     bool keep[2];
     uint32_t mk[2];
     int pg[2];
+    bool long_run = false;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int e = 32 * r + lane;
       const uint32_t k = v[r];
       const bool valid = k != 0xFFFFFFFFu;
-      const bool first = valid && (e == 0 || (tail->sorted[e - 1] >> 2) != (k >> 2));
+      if (valid && prev[r] == k && split == 0)  // the same block twice in one token's list
+        flag_error(p.err, MSA_ERR_TOPK_DUP);
+      const bool first = valid && (prev[r] == 0xFFFFFFFFu || (prev[r] >> 2) != (k >> 2));
       uint32_t m = 0;
       if (first) {
-        for (int f = e; f < kMaxUnion; ++f) {   // the run of this block's keys
-          const uint32_t kf = tail->sorted[f];
-          if (kf == 0xFFFFFFFFu || (kf >> 2) != (k >> 2)) break;
-          if (m & (1u << (kf & 3))) {   // the same block twice in one token's list
-            if (split == 0) flag_error(p.err, MSA_ERR_TOPK_DUP);
-          }
-          m |= 1u << (kf & 3);
+        m = 1u << (k & 3);
+        bool same = true;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+          const uint32_t kf = nxt[r][d];
+          same = same && kf != 0xFFFFFFFFu && (kf >> 2) == (k >> 2);
+          if (same && d < 3) m |= 1u << (kf & 3);
+          if (same && d == 3) long_run = true;   // five or more keys: duplicates
         }
       }
       int page = -1;
@@ -392,6 +413,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       keep[r] = ok;
       mk[r] = m;
       pg[r] = page;
+    }
+    if (__any_sync(0xffffffffu, long_run)) {
+      // a list with duplicates: each run's tokens from the whole sorted sequence
+      tail->sorted[lane] = v[0];
+      tail->sorted[32 + lane] = v[1];
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (!keep[r]) continue;
+        const uint32_t k = v[r];
+        uint32_t m = 0;
+        for (int f = 32 * r + lane; f < kMaxUnion; ++f) {
+          const uint32_t kf = tail->sorted[f];
+          if (kf == 0xFFFFFFFFu || (kf >> 2) != (k >> 2)) break;
+          m |= 1u << (kf & 3);
+        }
+        mk[r] = m;
+      }
+      __syncwarp();
     }
     const unsigned b0 = __ballot_sync(0xffffffffu, keep[0]);
     const unsigned b1 = __ballot_sync(0xffffffffu, keep[1]);
