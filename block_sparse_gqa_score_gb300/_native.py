@@ -25,7 +25,7 @@ EXPORTS = ("msa_score", "msa_topk", "msa_workspace_bytes", "msa_choose_splits",
            "msa_sparse_decode_select_q8", "msa_dense_decode_q8", "msa_sparse_prefill",
            "msa_sparse_prefill_select", "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
            "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
-           "msa_set_input_overlap", "msa_set_union_tile")
+           "msa_set_input_overlap", "msa_set_union_tile", "msa_test_wait_timeout")
 
 _lib = None
 _lock = threading.Lock()
@@ -93,6 +93,7 @@ def load(path: str | None = None):
                                         i32, i32, i64, f32, f32, f32, i32, P]
         lib.msa_set_input_overlap.argtypes = [i32]
         lib.msa_set_union_tile.argtypes = [i32]
+        lib.msa_test_wait_timeout.argtypes = [ctypes.c_ulonglong, P]
         lib.msa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.msa_strerror.argtypes = [i32]
         lib.msa_strerror.restype = ctypes.c_char_p
@@ -103,7 +104,7 @@ def load(path: str | None = None):
                      "msa_dense_decode_q8", "msa_sparse_prefill", "msa_sparse_prefill_select",
                      "msa_sparse_prefill_q8", "msa_sparse_prefill_select_q8",
                      "msa_score_kcache", "msa_score_kcache_q8", "msa_decode_step",
-                     "msa_set_input_overlap", "msa_set_union_tile"):
+                     "msa_set_input_overlap", "msa_set_union_tile", "msa_test_wait_timeout"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -612,6 +612,15 @@ int msa_decode_step(const void* q, float q_scale, const void* kv, const void* in
   return enqueue_attend(L, s, true);
 }
 
+int msa_test_wait_timeout(unsigned long long limit_ns, msa_stream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 2000000000ull) return MSA_EINVAL;
+  DeviceState* dev;
+  const int st = device_state(&dev);
+  if (st != MSA_OK) return st;
+  return from_cuda(
+      msa::launch_wait_timeout(limit_ns, dev->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int msa_set_union_tile(int enable) {
   return g_union_tile.exchange(enable ? 1 : 0, std::memory_order_relaxed);
 }

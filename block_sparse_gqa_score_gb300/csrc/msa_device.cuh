@@ -138,7 +138,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned pari
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
+// Wait for phase `parity` of `bar` to complete, for at most limit_ns
+// (mbar_wait: kWaitLimitNs).
 // The first two tries carry no suspend-time hint: on the kernels' per-page
 // hand-offs (TMA -> MMA -> softmax -> MMA) they return sooner after the phase
 // completes than a hinted try does (the batch-16, qlen-4 step 69.3 vs 70.3 us,
@@ -146,14 +147,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned pari
 // with a 1 ms hint, leaving the issue slots to the warps doing work (polling
 // with test_wait instead cost 17 us per step).  Returns false on timeout (the
 // caller flags MSA_ERR_TIMEOUT and bails out).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, unsigned parity,
+                                                unsigned long long limit_ns) {
   constexpr unsigned kHintNs = 1000000u;  // re-check the time limit every 1 ms at most
   if (mbar_try_wait(bar, parity) || mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
+  const unsigned hint = limit_ns < kHintNs ? static_cast<unsigned>(limit_ns) : kHintNs;
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  return mbar_wait_limit(bar, parity, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------------

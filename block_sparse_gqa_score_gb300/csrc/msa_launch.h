@@ -123,6 +123,9 @@ cudaError_t launch_union_attend(const CUtensorMap& kv_map, const AttendParams& p
 int union_ctas_per_unit(int units, int sm_count);
 constexpr int kUnionTile = 4;   // query tokens per union tile
 
+// The bounded-wait exit exercised on purpose (msa_waittest.cu).
+cudaError_t launch_wait_timeout(unsigned long long limit_ns, unsigned* err, cudaStream_t stream);
+
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
                            int splits, cudaStream_t stream, bool pdl);
 

@@ -474,6 +474,19 @@ int msa_set_union_tile(int enable);
 int msa_set_input_overlap(int enable);
 
 /*
+ * msa_test_wait_timeout -- for tests of the failure path.  Every wait inside
+ * the library's kernels is bounded (2 s): when a phase does not complete in
+ * time, the kernel sets MSA_ERR_TIMEOUT in the error word, waits (bounded)
+ * for the copies it has in flight, frees its tensor memory and returns, so
+ * the context stays usable.  This call enqueues one small kernel that takes
+ * that exit on purpose: it allocates tensor memory, starts a bulk copy, and
+ * waits limit_ns on an mbarrier that nothing completes.  Afterwards
+ * msa_get_error reports MSA_ERR_TIMEOUT and later calls work as usual.
+ * limit_ns in [1000, 2e9]; MSA_EINVAL otherwise.
+ */
+int msa_test_wait_timeout(unsigned long long limit_ns, msa_stream_t stream);
+
+/*
  * Read the current device's sticky error word (an OR of MSA_ERR_* bits set by
  * any earlier call on any stream) into *flags, and reset it when `clear` is
  * non-zero.  Synchronises the device first.  Returns MSA_OK or MSA_ECUDA.

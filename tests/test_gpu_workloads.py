@@ -107,19 +107,26 @@ def _prefill_full_size(inp, rng):
     assert_out_close(o_gpu[rows], o_ref)
 
 
-@pytest.mark.parametrize("name", ["b16_q4_h64kv4_8k-32k", "b128_q1_h64kv4_lognormal16k_pad10"])
-def test_workload_selection_end_to_end(name):
+@pytest.mark.parametrize("name,n_units", [
+    ("b16_q4_h64kv4_8k-32k", 3),
+    ("b128_q1_h64kv4_lognormal16k_pad10", 3),
+    ("b2_q32_h64kv4_256k_outliers", 8),      # every unit of the workload
+    ("b16_q32_h64kv4_256k_outliers", 8),
+])
+def test_workload_selection_end_to_end(name, n_units):
     """Selection from the GPU's scores vs from the oracle's fp64 scores on whole
     (request, KV head) units: identical except where the oracle's gap between
-    the 15th and 16th candidate is within the score tolerance."""
+    the 15th and 16th candidate is within the score tolerance.  The 256k
+    workloads with outlier keys rank 2048 candidates per token, 32 tokens per
+    request."""
     inp = wl.make_inputs(name, device=DEV)
     scores, topk, _ = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.qlen,
                                       inp.sm_scale, inp.k_scale, inp.v_scale)
     p = to_problem(inp, oracle)
     rng = np.random.default_rng(5)
-    live = [b for b in range(inp.batch) if inp.seq_lens_list[b] > 0]
-    units = [int(rng.choice(live)) * inp.num_kv_heads + int(rng.integers(inp.num_kv_heads))
-             for _ in range(3)]
+    live = [b * inp.num_kv_heads + g for b in range(inp.batch) if inp.seq_lens_list[b] > 0
+            for g in range(inp.num_kv_heads)]
+    units = sorted(int(u) for u in rng.choice(live, size=min(n_units, len(live)), replace=False))
     s_ref = oracle.score_units(p, units)
     t_gpu = topk.cpu().numpy()
     mismatches, near_ties = 0, 0
