@@ -48,6 +48,8 @@ constexpr int kRedSlots = 8;        // pages in flight between the epilogue warp
 constexpr int kQmulRing = 16;       // units whose scale factors are kept (> nqb + nacc + kRedSlots)
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kSmemPerSM = 233472;  // shared memory of one SM available to CTAs
+static_assert(kMaxStages <= 32 && kMaxAcc <= 32 && kRedSlots <= 32 && kQmulRing <= 32,
+              "one lane initialises each barrier of a ring");
 
 struct ScoreTail {
   uint64_t full[kMaxStages];   // TMA -> MMA
@@ -69,6 +71,8 @@ struct ScoreTail {
 
 struct ScoreGeometry {
   int Q, nh, Qu, nacc, ncols, nqb, stages, per_sm;
+  int fuse;     // a bf16 query's hi and lo parts in one MMA (N = 32 Qu), summed by the epilogue
+  int ucols;    // accumulator columns of one unit: 16 Qu, or 32 Qu when fused
   int nsub;     // epilogue warps per TMEM lane quarter (2 with one CTA per SM)
   int threads;  // 32 * (8 + 4 * (nsub - 1))
   int qtile_bytes;  // hi + lo query tiles of one unit: 2 x 16Q rows x 128 B
@@ -77,13 +81,21 @@ struct ScoreGeometry {
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-__host__ __device__ inline ScoreGeometry score_geometry(int Q) {
+__host__ __device__ inline ScoreGeometry score_geometry(int Q, bool fp8) {
   ScoreGeometry G{};
   G.Q = Q;
   G.nh = (16 * Q > 256) ? 2 : 1;        // MMA N is at most 256: split the tokens in two
   G.Qu = (Q + G.nh - 1) / G.nh;         // tokens per accumulator unit
-  G.nacc = (kMaxAcc * 16 * G.Qu <= 256) ? kMaxAcc : 2;   // accumulator buffers
-  int cols = G.nacc * 16 * G.Qu;
+  // Up to qlen 2 the hi and lo query tiles, adjacent in shared memory, form
+  // one B operand of N = 32 Qu <= 64: the K tile is read once per k-step
+  // instead of twice, and the two parts land in separate columns (batch 128,
+  // qlen 1: scorer 232 -> 215 us).  At qlen 4 the wider accumulators would
+  // leave room for two buffers instead of four, which measured slower
+  // (43.3 vs 40.9 us at batch 16).
+  G.fuse = (!fp8 && kMaxAcc * 32 * G.Qu <= 256) ? 1 : 0;
+  G.ucols = (G.fuse ? 32 : 16) * G.Qu;
+  G.nacc = (kMaxAcc * G.ucols <= 256) ? kMaxAcc : 2;   // accumulator buffers
+  int cols = G.nacc * G.ucols;
   int nc = 32;
   while (nc < cols) nc <<= 1;
   G.ncols = nc;
@@ -122,6 +134,15 @@ __host__ __device__ inline ScoreGeometry score_geometry(int Q) {
 // query buffer, and the tile's raw rows (Q tokens x 16 rows) fit in a stage.
 __host__ __device__ inline bool stage_staging(const ScoreGeometry& G, bool fp8) {
   return G.nqb == 1 && G.Q * kGroup * (fp8 ? 128 : 256) <= kHalfTile;
+}
+
+// Where the first unit's raw query rows are staged: the second tile buffer
+// (free until the second tile is built) or, with one buffer, the last K
+// stage (which the producer loads only once the first tile is built).
+__device__ __forceinline__ uint8_t* first_tile_staging(const ScoreGeometry& G, bool fp8,
+                                                       uint8_t* stages, uint8_t* qtiles) {
+  return G.nqb == 2 ? qtiles + G.qtile_bytes
+         : stage_staging(G, fp8) ? stages + (G.stages - 1) * kHalfTile : nullptr;
 }
 
 __device__ __forceinline__ int order_int(float x) {
@@ -196,17 +217,20 @@ __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk&
 // Query tile of unit (b, g) into hi / lo (16 Q rows x 128 B each, 128B
 // swizzled, K-major), per-token factors into qmul[0..Q): a bf16 query scaled
 // by 2^-e and split exactly into hi + lo (factor scale * 2^e), or an fp8 query
-// as stored in hi (lo unused; factor scale * q_scale).  With `staging` (at
-// least Q * 4 KiB of shared memory nothing else uses meanwhile), every token's
-// rows are first copied there with asynchronous copies, all in flight at
-// once, so the tile costs one memory round trip instead of one per token.
+// as stored in hi (lo unused; factor scale * q_scale).  The calling warp
+// builds tokens j0, j0 + jstep, ... (each token's scale is its own).  With
+// `staging` (Q * 4 KiB of shared memory nothing else uses meanwhile), those
+// tokens' rows are first copied there with asynchronous copies, all in flight
+// at once, so that the tile costs one memory round trip instead of one per
+// token.
 template <bool kFp8Q>
 __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
-                                   float* qmul, int lane, uint8_t* staging) {
+                                   float* qmul, int lane, uint8_t* staging, int j0 = 0,
+                                   int jstep = 1) {
   constexpr int kRowBytes = kFp8Q ? 128 : 256;   // one query head's row
   constexpr int kTokBytes = kGroup * kRowBytes;  // one token's 16 rows, contiguous
   if (staging) {
-    for (int jq = 0; jq < p.Q; ++jq) {
+    for (int jq = j0; jq < p.Q; jq += jstep) {
       const int64_t row = (static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup;
       const uint8_t* src = kFp8Q ? p.q8 + row * kHeadDim
                                  : reinterpret_cast<const uint8_t*>(p.q + row * kHeadDim);
@@ -219,7 +243,7 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     __syncwarp();
   }
-  for (int jq = 0; jq < p.Q; ++jq) {
+  for (int jq = j0; jq < p.Q; jq += jstep) {
     const int64_t row = (static_cast<int64_t>(b) * p.Q + jq) * p.Hq + g * kGroup;
     if constexpr (kFp8Q) {
       if (staging) {
@@ -264,7 +288,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int Q = p.Q;
-  const ScoreGeometry G = score_geometry(Q);
+  const ScoreGeometry G = score_geometry(Q, kFp8Q);
   uint8_t* stages = smem;                                              // [stages][128][128 B]
   uint8_t* qtiles = smem + G.off_q;                                    // [nqb][hi, lo][16Q][128 B]
   float* qmul_ring = reinterpret_cast<float*>(smem + G.off_qmul);      // [kQmulRing][Q]
@@ -273,6 +297,40 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int T = p.B * Q;
   const int qtile_half = G.qtile_bytes / 2;
+
+  // Tensor memory first: the hardware places a second CTA of this kernel on
+  // the SM only once the first has relinquished its allocation permit
+  // (allocating after the prefix sum below started the second CTA of every SM
+  // 2 us after the first).
+  if (warp == 1) {
+    tc::tmem_alloc(&tail->tmem_base, G.ncols);
+    tc::tmem_relinquish();
+  } else if (warp == 0) {
+    // the pipeline's barriers, spread over the lanes
+    if (lane < G.stages) {
+      mbar_init(&tail->full[lane], 1);
+      mbar_init(&tail->empty[lane], 1);
+    }
+    if (lane < kMaxAcc) {
+      mbar_init(&tail->dfull[lane], 1);
+      mbar_init(&tail->dempty[lane], 4 * kSub);
+    }
+    if (lane < 2) {
+      mbar_init(&tail->qfull[lane], 1);
+      mbar_init(&tail->qempty[lane], 1);
+    }
+    if (lane < kRedSlots) {
+      mbar_init(&tail->red_full[lane], 4 * kSub);
+      mbar_init(&tail->red_empty[lane], 1);
+    }
+    if (lane < kQmulRing) mbar_init(&tail->qmul_ready[lane], 1);
+    if (lane == 0) {
+      mbar_init(&tail->qstage, 1);
+      mbar_init(&tail->finish, kNumThreads / 32);
+      tail->any_invalid = 0;
+    }
+    fence_barrier_init();
+  }
 
   // ---- this CTA's page range: block-wide prefix sum over the requests -----------
   {
@@ -314,37 +372,29 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       }
     }
   }
-  if (warp == 0 && lane == 0) {
-    for (int s = 0; s < G.stages; ++s) {
-      mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], 1);
-    }
-    for (int s = 0; s < kMaxAcc; ++s) {
-      mbar_init(&tail->dfull[s], 1);
-      mbar_init(&tail->dempty[s], 4 * kSub);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&tail->qfull[s], 1);
-      mbar_init(&tail->qempty[s], 1);
-    }
-    for (int s = 0; s < kRedSlots; ++s) {
-      mbar_init(&tail->red_full[s], 4 * kSub);
-      mbar_init(&tail->red_empty[s], 1);
-    }
-    for (int s = 0; s < kQmulRing; ++s) mbar_init(&tail->qmul_ready[s], 1);
-    mbar_init(&tail->qstage, 1);
-    mbar_init(&tail->finish, kNumThreads / 32);
-    tail->any_invalid = 0;
-    fence_barrier_init();
-  } else if (warp == 1) {
-    tc::tmem_alloc(&tail->tmem_base, G.ncols);
-    tc::tmem_relinquish();
-  }
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
   const int count = tail->count;
   const uint32_t tmem = tail->tmem_base;
+
+  // The first query tile, which the first products wait for, is built by
+  // warps 2-6 together, a token each in turn (converting one token's 16 rows
+  // to e4m3 hi + lo takes one warp about a microsecond); warp 2 publishes it.
+  const int nq0 = Q < 5 ? Q : 5;
+  if (count > 0 && warp >= 2 && warp < 2 + nq0) {
+    PageWalk w0;
+    w0.begin(p, tail->start_b, tail->start_rem);
+    prepare_query_tile<kFp8Q>(p, w0.b, w0.g, qtiles, qtiles + qtile_half, qmul_ring, lane,
+                              first_tile_staging(G, kFp8Q, stages, qtiles), warp - 2, nq0);
+    tc::fence_proxy_async_smem();   // read by the tensor core (and the staging rewritten by TMA)
+    named_barrier(3, 32 * nq0);
+    if (warp == 2 && lane == 0) {
+      mbar_arrive(&tail->qfull[0]);
+      mbar_arrive(&tail->qmul_ready[0]);
+      mbar_arrive(&tail->qstage);
+    }
+  }
 
   // Warps 1 and 3-7 check every block-table entry of the range once, in
   // parallel, while warp 0 starts streaming and warp 2 prepares the first
@@ -414,7 +464,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       const uint64_t bdesc0 = tc::sw128_kmajor_desc(smem_u32(qtiles));
       const uint64_t lo_step = static_cast<uint64_t>(qtile_half >> 4);
       uint32_t idesc[2];
-      for (int h = 0; h < 2; ++h) idesc[h] = tc::idesc_e4m3_f32(128, 16 * max(1, min(G.Qu, Q - h * G.Qu)));
+      for (int h = 0; h < 2; ++h)
+        idesc[h] = tc::idesc_e4m3_f32(128, (G.fuse ? 32 : 16) * max(1, min(G.Qu, Q - h * G.Qu)));
       PageWalk w;
       if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
       int k = -1, pb = -1, pg = -1, vp = 0;
@@ -455,11 +506,11 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
             }
             tc::fence_after_thread_sync();
           }
-          const uint32_t d = tmem + buf * 16 * G.Qu;
+          const uint32_t d = tmem + buf * G.ucols;
           const uint64_t bh = bq + static_cast<uint64_t>((h * G.Qu * kGroup * 128) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bh + 2 * ks, idesc[h], ks > 0);
-          if constexpr (!kFp8Q) {  // the lo part of a bf16 query adds into the same columns
+          if (!kFp8Q && !G.fuse) {  // the lo part of a bf16 query adds into the same columns
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
@@ -483,29 +534,22 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     int t = 0, k = 0;
     bool ok = true;
     while (t < count && ok) {
-      const int qb = k % G.nqb;
-      if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], ((k / G.nqb) - 1) & 1)) {
-        if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
-        ok = false;
-        break;
-      }
-      uint8_t* qhi = qtiles + qb * G.qtile_bytes;
-      float* qmul = qmul_ring + (k % kQmulRing) * Q;
-      // the first tile, which the first products wait for, is staged through
-      // the second tile buffer (free until the second tile is built), or with
-      // a single buffer through the last K stage, which the producer loads
-      // only once this tile is built
-      uint8_t* staging = k != 0 ? nullptr
-                         : G.nqb == 2 ? qtiles + G.qtile_bytes
-                         : stage_staging(G, kFp8Q) ? stages + (G.stages - 1) * kHalfTile
-                                                   : nullptr;
-      prepare_query_tile<kFp8Q>(p, w.b, w.g, qhi, qhi + qtile_half, qmul, lane, staging);
-      tc::fence_proxy_async_smem();   // the tile is read by the tensor core (and the staging rewritten by TMA)
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&tail->qfull[qb]);
-        mbar_arrive(&tail->qmul_ready[k % kQmulRing]);
-        if (k == 0) mbar_arrive(&tail->qstage);
+      if (k > 0) {   // the first tile is built above
+        const int qb = k % G.nqb;
+        if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], ((k / G.nqb) - 1) & 1)) {
+          if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        uint8_t* qhi = qtiles + qb * G.qtile_bytes;
+        prepare_query_tile<kFp8Q>(p, w.b, w.g, qhi, qhi + qtile_half,
+                                  qmul_ring + (k % kQmulRing) * Q, lane, nullptr);
+        tc::fence_proxy_async_smem();   // the tile is read by the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tail->qfull[qb]);
+          mbar_arrive(&tail->qmul_ready[k % kQmulRing]);
+        }
       }
       // skip to the first page of the next unit
       const int in_unit = w.nhi - w.n;
@@ -563,6 +607,25 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
         }
         tc::fence_after_thread_sync();
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
+        const uint32_t acc = lane_addr + buf * G.ucols;
+        if (!kFp8Q && G.fuse) {
+          // token by token: its hi columns (16 j) and lo columns (16 Qu + 16 j),
+          // summed head by head before the maximum
+          for (int j = sub; j < ntok; j += kSub) {
+            const int lim = lim_base + tok0 + j;
+            if (lim < 0) continue;                 // warp-uniform: nothing visible
+            uint32_t vh[16], vl[16];
+            tc::ld_32x32b_x16(acc + j * 16, vh);
+            tc::ld_32x32b_x16(acc + 16 * G.Qu + j * 16, vl);
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              vh[c] = __float_as_uint(__uint_as_float(vh[c]) + __uint_as_float(vl[c]));
+            const int ord = __reduce_max_sync(0xffffffffu,
+                                              order_int(key <= lim ? max16(vh) : -INFINITY));
+            if (lane == tok0 + j) myv = order_float(ord);
+          }
+        } else
         // groups of four tokens: four TMEM loads in flight under one wait, then
         // four independent tree maxima and four back-to-back warp reductions
         for (int j0 = kGrp * sub; j0 < ntok; j0 += kGrp * kSub) {
@@ -571,7 +634,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
           uint32_t v[kGrp][16];
 #pragma unroll
           for (int jj = 0; jj < kGrp; ++jj)
-            if (jj < nj) tc::ld_32x32b_x16(lane_addr + buf * 16 * G.Qu + (j0 + jj) * 16, v[jj]);
+            if (jj < nj) tc::ld_32x32b_x16(acc + (j0 + jj) * 16, v[jj]);
           tc::wait_ld();
           int ord[kGrp];
 #pragma unroll
@@ -659,7 +722,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
 cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream,
                          bool pdl) {
   if (p.ctas < 1) return cudaErrorInvalidValue;
-  const ScoreGeometry G = score_geometry(p.Q);
+  const ScoreGeometry G = score_geometry(p.Q, p.q8 != nullptr);
   if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {

@@ -36,11 +36,7 @@ __global__ void __launch_bounds__(64) wait_timeout_kernel(unsigned long long lim
   tc::fence_after_thread_sync();
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&landed, sizeof(buf));
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(buf)), "l"(g_wait_src), "r"(static_cast<unsigned>(sizeof(buf))),
-        "r"(smem_u32(&landed))
-        : "memory");
+    bulk_load(buf, g_wait_src, sizeof(buf), &landed);
     if (!mbar_wait_limit(&never, 0, limit_ns)) {
       flag_error(err, MSA_ERR_TIMEOUT);
       // the exit every kernel takes: the copies in flight land first
