@@ -223,10 +223,13 @@ __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk&
 // tokens' rows are first copied there with asynchronous copies, all in flight
 // at once, so that the tile costs one memory round trip instead of one per
 // token.
-template <bool kFp8Q>
+template <bool kFp8Q, bool kShared = false>
 __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* qhi, uint8_t* qlo,
-                                   float* qmul, int lane, uint8_t* staging, int j0 = 0,
-                                   int jstep = 1) {
+                                   float* qmul, int lane, uint8_t* staging, int j0_ = 0,
+                                   int jstep_ = 1) {
+  // kShared: several warps build the tile, this one tokens j0, j0 + jstep, ...;
+  // otherwise all tokens, in a plain loop
+  const int j0 = kShared ? j0_ : 0, jstep = kShared ? jstep_ : 1;
   constexpr int kRowBytes = kFp8Q ? 128 : 256;   // one query head's row
   constexpr int kTokBytes = kGroup * kRowBytes;  // one token's 16 rows, contiguous
   if (staging) {
@@ -298,11 +301,13 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   const int T = p.B * Q;
   const int qtile_half = G.qtile_bytes / 2;
 
-  // Tensor memory first: the hardware places a second CTA of this kernel on
-  // the SM only once the first has relinquished its allocation permit
+  // Tensor memory first when two CTAs share an SM: the hardware places the
+  // second CTA only once the first has relinquished its allocation permit
   // (allocating after the prefix sum below started the second CTA of every SM
-  // 2 us after the first).
-  if (warp == 1) {
+  // 2 us after the first).  With one CTA per SM it is allocated after the
+  // prefix sum, which keeps the wide instantiation free of spills (allocated
+  // first, its qlen-32 scorer spilled and took 1735 instead of 1591 us).
+  if (!kWide && warp == 1) {
     tc::tmem_alloc(&tail->tmem_base, G.ncols);
     tc::tmem_relinquish();
   } else if (warp == 0) {
@@ -372,6 +377,10 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       }
     }
   }
+  if (kWide && warp == 1) {
+    tc::tmem_alloc(&tail->tmem_base, G.ncols);
+    tc::tmem_relinquish();
+  }
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
@@ -385,8 +394,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   if (count > 0 && warp >= 2 && warp < 2 + nq0) {
     PageWalk w0;
     w0.begin(p, tail->start_b, tail->start_rem);
-    prepare_query_tile<kFp8Q>(p, w0.b, w0.g, qtiles, qtiles + qtile_half, qmul_ring, lane,
-                              first_tile_staging(G, kFp8Q, stages, qtiles), warp - 2, nq0);
+    prepare_query_tile<kFp8Q, true>(p, w0.b, w0.g, qtiles, qtiles + qtile_half, qmul_ring, lane,
+                                    first_tile_staging(G, kFp8Q, stages, qtiles), warp - 2, nq0);
     tc::fence_proxy_async_smem();   // read by the tensor core (and the staging rewritten by TMA)
     named_barrier(3, 32 * nq0);
     if (warp == 2 && lane == 0) {
@@ -510,7 +519,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
           const uint64_t bh = bq + static_cast<uint64_t>((h * G.Qu * kGroup * 128) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bh + 2 * ks, idesc[h], ks > 0);
-          if (!kFp8Q && !G.fuse) {  // the lo part of a bf16 query adds into the same columns
+          if (!kFp8Q && (kWide || !G.fuse)) {  // the lo part of a bf16 query adds into the same columns
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
@@ -608,7 +617,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
         tc::fence_after_thread_sync();
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
         const uint32_t acc = lane_addr + buf * G.ucols;
-        if (!kFp8Q && G.fuse) {
+        if (!kFp8Q && !kWide && G.fuse) {   // (fused only at qlen <= 2: two CTAs per SM)
           // token by token: its hi columns (16 j) and lo columns (16 Qu + 16 j),
           // summed head by head before the maximum
           for (int j = sub; j < ntok; j += kSub) {
