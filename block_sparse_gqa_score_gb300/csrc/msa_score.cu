@@ -18,12 +18,14 @@
 //    request's Q x 16 query rows as operand B (N = 16 Q), accumulating fp32 in
 //    two or four tensor-memory accumulator buffers;
 //  * warp 2 prepares the query tile of each (request, KV head) unit of the
-//    range: the bf16 query, scaled per token by a power of two 2^-e, is
-//    represented exactly as the sum of two fp8 e4m3 parts (bf16's 8
-//    significant bits are 4 + 4) that accumulate into the same columns, so
-//    the fp8 keys need no widening (an fp8 query, value q8 * q_scale, is the
-//    hi part as stored and only its MMAs are issued: half the tensor work);
-//    it also writes the -inf tails;
+//    range (the first one together with warps 3-6, a token each): the bf16
+//    query, scaled per token by a power of two 2^-e, is represented exactly
+//    as the sum of two fp8 e4m3 parts (bf16's 8 significant bits are 4 + 4)
+//    that accumulate into the same columns (up to qlen 2: side by side as one
+//    B operand of N = 32 Q, summed by the epilogue), so the fp8 keys need no
+//    widening (an fp8 query, value q8 * q_scale, is the hi part as stored and
+//    only its MMAs are issued: half the tensor work); it also writes the -inf
+//    tails;
 //  * warps 3-6 read the accumulator (one key per lane), take each token's max
 //    over its 16 heads and visible keys, and publish their four quarter-page
 //    maxima through shared memory and a per-slot mbarrier; with one CTA per
