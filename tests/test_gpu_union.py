@@ -132,3 +132,89 @@ def test_union_flags_bad_entries_per_token():
     assert flags & msa._native.ERR_TOPK_RANGE and flags & msa._native.ERR_TOPK_DUP
     ref = oracle.attend(to_problem(inp, oracle), clean.numpy())
     assert_out_close(_np(out), ref)
+
+
+def _fp8(inp):
+    """The query quantised per tensor (scale = amax / 448) and the oracle
+    problem for it: the fp8 codes as bf16 (exact) with sm_scale * q_scale."""
+    from tests.helpers import q_bits
+    qf = inp.q.float()
+    q_scale = float(qf.abs().max()) / 448.0
+    q8 = (qf / q_scale).to(torch.float8_e4m3fn)
+    p = oracle.Problem(q_bits(q8.to(torch.bfloat16)), inp.kv.cpu().numpy(),
+                       inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy(), inp.qlen,
+                       inp.num_q_heads, inp.num_kv_heads, inp.sm_scale * q_scale, inp.k_scale,
+                       inp.v_scale)
+    return q8, q_scale, p
+
+
+def test_union_fp8_query_matches_oracle():
+    """An fp8 query (value q8 * q_scale) through the union tile: the whole step
+    (selection inside the union kernel) and the attend on given lists."""
+    seq_lens, Q, Hq, Hkv = [7000, 260, 15000, 3], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=405, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    q8, qs, p = _fp8(inp)
+    scores, tk, out = msa.decode_step(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                                      inp.k_scale, inp.v_scale, q_scale=qs)
+    s_gpu = _np(scores)
+    assert np.array_equal(tk.cpu().numpy(),
+                          oracle.topk(s_gpu, np.array(seq_lens, dtype=np.int32), Q))
+    assert_out_close(_np(out), oracle.attend(p, tk.cpu().numpy()), padding_rows(seq_lens, Q))
+    given = wl.draw_topk_given(seq_lens, Q, Hkv, torch.Generator().manual_seed(6))
+    out2 = msa.sparse_decode(q8, inp.kv, inp.block_table, inp.seq_lens, given.to(DEV), Q,
+                             inp.sm_scale, inp.k_scale, inp.v_scale, num_splits=3, q_scale=qs)
+    assert_out_close(_np(out2), oracle.attend(p, given.numpy()), padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
+
+
+def test_union_step_agrees_with_the_per_token_step():
+    """The whole step with and without the union tile: the same scores and
+    lists (the scorer and selector are shared), outputs that both match the
+    oracle."""
+    seq_lens, Q, Hq, Hkv = [9000, 4100, 20000, 128], 4, 64, 4
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=406, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    s_u, tk_u, out_u = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q,
+                                       inp.sm_scale, inp.k_scale, inp.v_scale)
+    msa.set_union_tile(False)
+    s_t, tk_t, out_t = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q,
+                                       inp.sm_scale, inp.k_scale, inp.v_scale)
+    assert torch.equal(s_u, s_t)
+    assert torch.equal(tk_u, tk_t)
+    ref = oracle.attend(to_problem(inp, oracle), tk_t.cpu().numpy())
+    assert_out_close(_np(out_u), ref, padding_rows(seq_lens, Q))
+    assert_out_close(_np(out_t), ref, padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
+
+
+def test_union_graph_replay_after_inputs_change():
+    """The union attend captured once in a CUDA graph (fixed split count and
+    workspace), replayed after the lengths, the lists and the query change in
+    place: the oracle's result on the new inputs."""
+    Q, Hq, Hkv, splits = 4, 32, 2, 2
+    lens_a, lens_b = [9000, 3000, 12000], [4000, 12800, 131]
+    inp = wl.make_custom(lens_a, Q, Hq, Hkv, seed=407, device=DEV, kv_std=0.5, min_stride=110)
+    lists = wl.draw_topk_given(lens_a, Q, Hkv, torch.Generator().manual_seed(7)).to(DEV)
+    out = torch.empty_like(inp.q)
+    ws = torch.empty(msa.workspace_bytes(3, Q, Hq, splits) or 1, dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, lists, Q, inp.sm_scale,
+                          inp.k_scale, inp.v_scale, out=out, num_splits=splits, workspace=ws)
+        with torch.cuda.graph(graph, stream=s):
+            msa.sparse_decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, lists, Q,
+                              inp.sm_scale, inp.k_scale, inp.v_scale, out=out,
+                              num_splits=splits, workspace=ws)
+    torch.cuda.synchronize()
+    inp.seq_lens.copy_(torch.tensor(lens_b, dtype=torch.int32))
+    lists.copy_(wl.draw_topk_given(lens_b, Q, Hkv, torch.Generator().manual_seed(8)))
+    inp.q.copy_(torch.randn(inp.q.shape, generator=torch.Generator().manual_seed(9)).to(inp.q))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    p = to_problem(inp, oracle)
+    assert_out_close(_np(out), oracle.attend(p, lists.cpu().numpy()), padding_rows(lens_b, Q))
+    assert msa.get_error() == 0
