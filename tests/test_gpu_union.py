@@ -4,7 +4,9 @@ which shares each page among a request's tokens (one pass over the union of a
 oracle's attend on the same lists: lists of one request that are identical,
 disjoint or partly overlapping, lists without the current block, tokens whose
 positions straddle a block boundary, partial tiles (Q = 2, 3, 5, 7), padding
-rows, and split counts from 1 to more than the union has pages."""
+rows, split counts from 1 to more than the union has pages, an fp8 query,
+the whole step against the per-token step, and a CUDA graph replayed after
+its inputs change."""
 from __future__ import annotations
 
 import numpy as np
