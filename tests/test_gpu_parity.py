@@ -626,3 +626,24 @@ def test_prefill_many_requests(B):
                              topk.to(DEV), inp.sm_scale, num_splits=2)
     assert_out_close(_np(out), prefill_oracle(inp, oracle, topk))
     assert msa.get_error() == 0
+
+
+@pytest.mark.parametrize("B,Q,Hq,Hkv", [(1100, 1, 16, 1), (300, 4, 32, 2), (200, 8, 16, 1)])
+def test_step_with_many_requests(B, Q, Hq, Hkv):
+    """Batches of hundreds of short requests (empty ones among them): the
+    scorer's prefix sum over the requests then takes several requests per
+    thread (and, at qlen 8, runs in the one-CTA-per-SM shape), the pages of a
+    CTA span many requests, and most rows have fewer than 16 candidates."""
+    gen = np.random.default_rng(B + Q)
+    seq_lens = [int(x) for x in gen.integers(0, 2600, size=B)]
+    seq_lens[:5] = [0, 1, 128, 129, 2048]
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=121 + Q, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    scores, tk, out = msa.decode_step(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q,
+                                      inp.sm_scale, inp.k_scale, inp.v_scale)
+    p = to_problem(inp, oracle)
+    s_gpu = _np(scores).astype(np.float64)
+    assert_scores_close(s_gpu, oracle.score(p))
+    assert np.array_equal(_np(tk), oracle.topk(s_gpu, np.array(seq_lens, dtype=np.int32), Q))
+    assert_out_close(_np(out), oracle.attend(p, _np(tk)), padding_rows(seq_lens, Q))
+    assert msa.get_error() == 0
