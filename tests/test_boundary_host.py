@@ -236,3 +236,22 @@ def test_k_only_cache_scorer_rejects(lib):
     for qs in (0.0, -1.0, float("nan")):
         assert lib.msa_score_kcache_q8(A, qs, A, A, A, A, 16, 4, 64, 4, 8, 100, 0.088, 1.0,
                                        None) == EINVAL
+
+
+def test_wait_timeout_limit_checked_on_the_host(lib):
+    """msa_test_wait_timeout rejects limits outside [1 us, 2 s] before anything
+    reaches a device."""
+    for limit in (0, 999, 2_000_000_001, 2**63):
+        assert lib.msa_test_wait_timeout(limit, None) == _native.EINVAL
+
+
+def test_process_wide_switches_return_the_previous_setting(lib):
+    """msa_set_union_tile, msa_set_input_overlap: each returns the setting it
+    replaces (any non-zero argument turns it on), and both start off."""
+    for fn in (lib.msa_set_union_tile, lib.msa_set_input_overlap):
+        first = fn(0)
+        assert first == 0
+        assert fn(7) == 0
+        assert fn(1) == 1
+        assert fn(0) == 1
+        assert fn(0) == 0
