@@ -349,12 +349,12 @@ int prepare_attend(const void* q, const void* kv, const int32_t* block_table,
                : cu_q ? msa_choose_splits(T, 1, Hkv, dev->sm_count)
                       : msa_choose_splits(B, Q, Hkv, dev->sm_count);
   if (union_tile && dense_span > 0) {
-    // dense decode over the union: at most the caller's split count (which
-    // sized the workspace), at most one CTA per SM
+    // dense decode over the union.  Units that fill the SMs: one CTA each.
+    // Fewer: one CTA per SM, shared out by the units' blocks (the union
+    // launcher and kernel), up to the caller's split count (which sized the
+    // workspace) per unit.
     const int64_t units = static_cast<int64_t>(B) * ((Q + msa::kUnionTile - 1) / msa::kUnionTile) * Hkv;
-    const int z = msa::union_ctas_per_unit(units > INT_MAX ? INT_MAX : static_cast<int>(units),
-                                           dev->sm_count);
-    splits = splits < z ? splits : z;
+    if (units >= dev->sm_count) splits = 1;
   }
   const size_t need = msa_workspace_bytes(tb, tq, Hq, splits);
   if (splits > 1 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))

@@ -34,7 +34,10 @@
 // layers attend the whole page table) is the same kernel with every block a
 // token may see as its list: the tile's union is the blocks up to its last
 // token's current block, each token listing a prefix of it, so every page is
-// loaded once for the whole tile.
+// loaded once for the whole tile.  With fewer units than SMs the launch has
+// one CTA per SM and each unit takes CTAs in proportion to its blocks (the
+// requests' lengths differ), so that no CTA holds much more than its share;
+// a page's tokens then share one S^T and one O^T product and three commits.
 //
 // Warp roles (20 warps, one CTA per SM):
 //   0      union, page list, TMA producer (5-stage ring of 32 KiB K|V pages)
@@ -75,6 +78,10 @@ constexpr int kSBufs = 3;
 constexpr uint32_t kColAcc = kSBufs * kN;
 constexpr int kTmemCols = 512;
 constexpr int kMaxDenseBlocks = 2048;         // dense decode: blocks of one CTA's range
+// dense decode with fewer (request, tile, KV head) units than SMs and split
+// parts: one CTA per SM, shared out in the kernel among up to this many
+// (request, tile) units in proportion to their blocks
+constexpr int kBalancedTiles = 256;
 constexpr float kPShift = 8.f;                // P = 2^(x - m + kPShift)
 constexpr float kLazy = 0.5f;                 // m moves when a page exceeds it by more than this
 constexpr int kTableCopy = 512;               // block-table entries copied to shared memory
@@ -154,6 +161,88 @@ __device__ __forceinline__ void warp_sort64(uint32_t (&v)[2], int lane) {
   }
 }
 
+// Blocks a dense-decode unit (request, tile) attends: up to its last token's
+// current block (0 for a padding request or a tile of padding rows).
+__device__ __forceinline__ int dense_tile_blocks(const AttendParams& p, int tu, int ntiles) {
+  const int b = tu / ntiles, tile = tu - b * ntiles;
+  const int L = p.seq_lens[b];
+  const bool seq_ok = L >= 0 && (L == 0 || (L - 1) / kPage < p.S);
+  const int tok = min(kQt * tile + kQt - 1, p.Q - 1);
+  const int pos = seq_ok ? L - p.Q + tok : -1;
+  return pos >= 0 ? pos / kPage + 1 : 0;
+}
+
+struct DenseSlot {
+  int unit;    // (request, tile, KV head) unit, in blockIdx.x order of the plain grid; -1: none
+  int part;    // which of its equal block ranges
+  int nparts;  // how many ranges the unit is cut into
+};
+
+// Dense decode's work for this CTA.  With a grid of one CTA per unit and split
+// that is (blockIdx.x, blockIdx.y, gridDim.y).  With more CTAs than units (one
+// per SM, launch_union_attend) the units share them out by their blocks: unit u (n_u blocks)
+// takes z_u = min(ceil(n_u / T), splits) CTAs (at least one) for the smallest
+// T at which every unit's CTAs fit the grid, so that no CTA holds much more
+// than its share of the batch's pages; the CTAs go to the units in order, a
+// unit's KV heads in turn, each head's ranges in turn.  Every CTA computes the
+// same assignment from seq_lens (one warp, every lane the same result); CTAs
+// past the last unit's get none.
+__device__ DenseSlot dense_slot(const AttendParams& p, int ntiles, int lane) {
+  const int NT = p.B * ntiles, H = p.Hkv, Z = p.splits, C = static_cast<int>(gridDim.x);
+  if (C <= NT * H)
+    return DenseSlot{static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y),
+                     static_cast<int>(gridDim.y)};
+  constexpr int kPer = kBalancedTiles / 32;
+  int n[kPer];
+  int maxn = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int tu = 32 * k + lane;
+    n[k] = tu < NT ? dense_tile_blocks(p, tu, ntiles) : 0;
+    maxn = max(maxn, n[k]);
+  }
+  maxn = __reduce_max_sync(0xffffffffu, maxn);
+  auto parts = [&](int k, int T) { return min(max((n[k] + T - 1) / T, 1), Z); };
+  auto ctas = [&](int T) {
+    int s = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (32 * k + lane < NT) s += parts(k, T);
+    return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(s))) * H;
+  };
+  // at T = max(n) every unit takes one CTA per head, NT * H <= C (the host's rule)
+  int lo = 1, hi = max(maxn, 1);
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ctas(mid) <= C) hi = mid;
+    else lo = mid + 1;
+  }
+  const int c = static_cast<int>(blockIdx.x);
+  int run = 0;   // CTAs of the units before this group of 32
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int tu = 32 * k + lane;
+    const int zc = tu < NT ? parts(k, lo) : 0;
+    int incl = zc * H;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const int start = run + incl - zc * H;
+    const unsigned hit = __ballot_sync(0xffffffffu, zc > 0 && c >= start && c < start + zc * H);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const int st = __shfl_sync(0xffffffffu, start, src);
+      const int z = __shfl_sync(0xffffffffu, zc, src);
+      const int rel = c - st;
+      return DenseSlot{(32 * k + src) * H + rel / z, rel % z, z};
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return DenseSlot{-1, 0, 1};
+}
+
 // kFp8Q: an fp8 query (q8 * q_scale); kDense: dense decode (no lists);
 // each compiled separately.
 template <bool kFp8Q, bool kDense>
@@ -170,11 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* table_s = reinterpret_cast<int32_t*>(pbuf);   // prologue only
 
   const int ntiles = (p.Q + kQt - 1) / kQt;
-  const int g = blockIdx.x % p.Hkv;
-  const int tile = (blockIdx.x / p.Hkv) % ntiles;
-  const int b = blockIdx.x / (p.Hkv * ntiles);
-  const int split = blockIdx.y, nsplit = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int unit = static_cast<int>(blockIdx.x), split = static_cast<int>(blockIdx.y);
+  int nsplit = static_cast<int>(gridDim.y);
+  if constexpr (kDense) {
+    const DenseSlot ds = dense_slot(p, ntiles, lane);
+    if (ds.unit < 0) return;   // the whole CTA: no unit left for it
+    unit = ds.unit;
+    split = ds.part;
+    nsplit = ds.nparts;
+  }
+  const int g = unit % p.Hkv;
+  const int tile = (unit / p.Hkv) % ntiles;
+  const int b = unit / (p.Hkv * ntiles);
   const int32_t* trow = p.block_table + static_cast<int64_t>(b) * p.S;
   const int ncopy = p.S < kTableCopy ? p.S : kTableCopy;
 
@@ -204,7 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         mbar_init(&tail->full[s], 1);
-        mbar_init(&tail->empty[s], kQt);   // one release per token and use
+        // one release per token and use; dense decode: one per page (its
+        // tokens' joint O^T product)
+        mbar_init(&tail->empty[s], kDense ? 1 : kQt);
       }
       for (int j = 0; j < kQt; ++j) {
         for (int s = 0; s < kSBufs; ++s) {
@@ -576,11 +675,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_thread_sync();
         const uint32_t mask = slot_mask(t);
         const int others = kQt - __popc(mask);
-        if (others > 0) mbar_arrive_count(&tail->empty[s], static_cast<unsigned>(others));
+        if (!kDense && others > 0) mbar_arrive_count(&tail->empty[s], static_cast<unsigned>(others));
         const uint64_t a = ak0 + static_cast<uint64_t>(s) * (kStageBytes >> 4);
         // dense decode: the listing tokens are consecutive and all at their
         // t-th page (their lists are prefixes of the range), so one product
-        // covers them; otherwise one product per listing token
+        // covers them, with one commit (to the last token's barrier, which
+        // lists every page of the range and on which they all wait);
+        // otherwise one product per listing token
         const int j0 = __ffs(mask) - 1, j1 = 31 - __clz(mask);
         const bool joint = kDense && mask == ((2u << j1) - (1u << j0));
         if (joint) {
@@ -599,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc_m = tc::idesc_e4m3_f32(128, 32 * (j1 - j0 + 1));
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bj + 2 * ks, idesc_m, ks > 0);
-          for (int j = j0; j <= j1; ++j) tc::commit(&tail->s_full[j][b]);
+          tc::commit(&tail->s_full[j1][b]);
           continue;
         }
 #pragma unroll
@@ -657,10 +758,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_e4m3(d, a + 256 * kk, bp + ((4 * kPBlock) >> 4) * kk, idesc_m,
                          (t > 0 || kk > 0) ? 1u : 0u);
-          for (int j = j0; j <= j1; ++j) {
-            tc::commit(&tail->o_done[j][buf]);
-            tc::commit(&tail->empty[s]);    // token j is done with the page
-          }
+          // one commit for the tokens (the last token's barrier, on which
+          // they all wait) and one for the stage
+          tc::commit(&tail->o_done[j1][buf]);
+          tc::commit(&tail->empty[s]);
         }
       } else {
         int k[kQt], n[kQt];
@@ -724,6 +825,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // token that listed that page
     const int fix_tok = fix_slot >= 0 ? __ffs(slot_mask(fix_slot)) - 1 : -1;
     uint8_t* pj = pbuf + 256 * j;      // token j's P^T columns
+    // the barriers token j waits on for its products: its own, or in dense
+    // decode the last listing token's (it lists every page of the range, and
+    // the products it commits are the tokens' joint ones; the others' pages
+    // are a prefix of its, so no barrier runs two phases ahead of a wait)
+    const int jw = kDense ? max(0, 31 - __clz(slot_mask(0))) : j;
     float* mxj = mx_all + j * 2 * 4 * kGroup;
     float* lsum = lsum_all + j * 4 * kGroup;
     bool ok = true;
@@ -736,20 +842,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     float nref_h = INFINITY;
     float l[kGroup];
     fill(l, 0.f);
+    uint32_t sv[32];   // page k's S^T row (hi | lo columns)
     for (int k = 0; k < n_j && ok; ++k) {
       const int t = tok_slot(j, k), buf = k & 1, sb = k % kSBufs;
       const int s = t % kStages;
-      if (!mbar_wait(&tail->s_full[j][sb], (k / kSBufs) & 1)) {
+      if (!mbar_wait(&tail->s_full[jw][sb], (k / kSBufs) & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_thread_sync();
+      tc::ld_32x32b_x32(lane_addr + kN * sb, sv);
       // keys <= lim are visible to this token (none on a dense slot with a bad entry)
       const int lim = slot_bad(t) ? -1 : pos - slot_block(t) * kPage;
       float x[kGroup];
       {
-        uint32_t sv[32];
-        tc::ld_32x32b_x32(lane_addr + kN * sb, sv);
         tc::wait_ld();
         tc::fence_before_thread_sync();
         __syncwarp();
@@ -794,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the accumulator holds the earlier pages relative to the old m: once
           // their products are complete (page k - 1's, and with it the earlier
           // ones), rescale it; page k's product waits for this page's P^T
-          if (!mbar_wait(&tail->o_done[j][(k - 1) & 1], ((k - 1) >> 1) & 1)) {
+          if (!mbar_wait(&tail->o_done[jw][(k - 1) & 1], ((k - 1) >> 1) & 1)) {
             ok = false;
             break;
           }
@@ -841,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&tail->vfix);
       }
       // P^T buffer `buf` was last read by page k - 2's product
-      if (k >= 2 && !mbar_wait(&tail->o_done[j][buf], ((k >> 1) - 1) & 1)) {
+      if (k >= 2 && !mbar_wait(&tail->o_done[jw][buf], ((k >> 1) - 1) & 1)) {
         ok = false;
         break;
       }
@@ -854,12 +960,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->p_full[j][buf]);
     }
+    // no load is in flight here; with this wait the batch-16 dense decode
+    // measured 149 instead of 152 us (code placement)
+    tc::wait_ld();
 
     // the output: every O^T product complete, this thread's value dim of each head
     float o[kGroup];
     fill(o, 0.f);
     if (ok && n_j > 0) {
-      ok = mbar_wait(&tail->o_done[j][(n_j - 1) & 1], ((n_j - 1) >> 1) & 1);
+      ok = mbar_wait(&tail->o_done[jw][(n_j - 1) & 1], ((n_j - 1) >> 1) & 1);
       if (ok) {
         tc::fence_after_thread_sync();
         uint32_t av[32];
@@ -926,6 +1035,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h == key) lr = l[h];
           p.part_ml[(base + key) * 2] = -nref_h;  // m - kPShift; -inf for a head without keys
           p.part_ml[(base + key) * 2 + 1] = lr;
+          // dense decode: a unit cut into fewer ranges than the workspace's
+          // parts; its first range marks the rest empty for the merge
+          if (kDense && split == 0)
+            for (int s2 = nsplit; s2 < p.splits; ++s2) {
+              p.part_ml[(static_cast<int64_t>(s2) * rows + row0 + key) * 2] = -INFINITY;
+              p.part_ml[(static_cast<int64_t>(s2) * rows + row0 + key) * 2 + 1] = 0.f;
+            }
         }
       }
     } else if (!ok && lane == 0) {
@@ -961,7 +1077,16 @@ cudaError_t launch_union_attend(const CUtensorMap& kv_map, const AttendParams& p
   });
   if (e != cudaSuccess) return e;
   const int ntiles = (p.Q + kQt - 1) / kQt;
-  const dim3 grid(p.B * ntiles * p.Hkv, p.splits);
+  dim3 grid(p.B * ntiles * p.Hkv, p.splits);
+  if (p.dense_span > 0 && p.splits > 1 && p.B * ntiles <= kBalancedTiles) {
+    // dense decode on fewer units than SMs: one CTA per SM, shared out by the
+    // units' blocks in the kernel (dense_slot), up to `splits` parts per unit
+    int dev = 0, sms = 0;
+    cudaError_t r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r != cudaSuccess) return r;
+    if (p.B * ntiles * p.Hkv < sms) grid = dim3(sms, 1);
+  }
   const dim3 block(kThreads);
   if (p.dense_span > 0)
     return p.q8 ? launch_pdl(union_attend_kernel<true, true>, grid, block, kSmemBytes, stream,

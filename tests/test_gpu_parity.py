@@ -280,12 +280,17 @@ def test_attend_lists_without_the_current_block():
 
 DENSE_CASES = [
     ([2048, 3000], 1, 16, 1),                     # the tiny workload's shapes
-    ([129, 385, 0, 7], 4, 64, 4),                 # one split, padding rows
+    ([129, 385, 0, 7], 4, 64, 4),                 # units of 2, 4, 0 and 1 blocks, padding rows
     ([0, 2, 3, 130, 2048, 2049], 4, 16, 1),       # page boundaries
     ([2500, 700], 32, 16, 1),                     # qlen at its upper bound
-    ([20000, 9000, 40000], 4, 64, 4),             # 16 splits of 20 blocks
+    ([20000, 9000, 40000], 4, 64, 4),             # uneven units: 313 blocks in 16 parts, 71 in fewer
     ([70000], 2, 16, 1),                          # blocks past the prologue's table copy
     ([262144], 1, 16, 1),                         # the longest table: 16 splits of 128 blocks
+    # lengths from 1 to 260000 tokens and a padding request: the units share
+    # one CTA per SM by their blocks, from one part to the workspace's sixteen
+    ([1, 131072, 0, 5000, 260000, 128, 129], 3, 32, 2),
+    # more (request, tile, KV head) units than SMs: one CTA each
+    ([1000 + 37 * b for b in range(40)], 8, 32, 2),
 ]
 
 
