@@ -47,6 +47,12 @@ constexpr int kWideSub = 4;      // epilogue warp sets when one CTA runs per SM
 constexpr int kMaxAcc = 4;          // tensor-memory accumulator buffers
 constexpr int kMaxStages = 8;
 constexpr int kRedSlots = 8;        // pages in flight between the epilogue warps
+// A second unit that starts within this many pages of a CTA's range gets its
+// query tile in the prologue (bf16 query, two CTAs per SM), from the warps
+// that build the first one: built by the query warp alone (about a microsecond per token) it
+// came late, and the CTAs whose range crosses a unit boundary in its first
+// pages ran up to 6 us behind the rest (a page every 1.2-1.3 us, not 1.02).
+constexpr int kNearUnit = 8;
 constexpr int kQmulRing = 16;       // units whose scale factors are kept (> nqb + nacc + kRedSlots)
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kSmemPerSM = 233472;  // shared memory of one SM available to CTAs
@@ -210,6 +216,14 @@ struct PageWalk {
     } while (nhi == 0);
   }
 };
+
+// Whether the range's second unit (if any) starts within kNearUnit pages, so
+// that the prologue builds its tile too (two tile buffers only).
+__device__ __forceinline__ bool second_tile_early(const ScoreGeometry& G, const PageWalk& w0,
+                                                  int count) {
+  const int first_len = w0.nhi - w0.n;   // pages of the first unit in the range
+  return G.nqb == 2 && first_len < count && first_len <= kNearUnit;
+}
 
 __device__ __forceinline__ bool page_valid(const ScoreParams& p, const PageWalk& w, int& page) {
   page = p.block_table[static_cast<int64_t>(w.b) * p.S + w.n];
@@ -396,6 +410,16 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   if (count > 0 && warp >= 2 && warp < 2 + nq0) {
     PageWalk w0;
     w0.begin(p, tail->start_b, tail->start_rem);
+    if (!kFp8Q && !kWide && warp == 2 && second_tile_early(G, w0, count)) {
+      // the second unit's query rows into L2 for its tile (built below)
+      PageWalk w1 = w0;
+      w1.advance(p, w1.nhi - w1.n);
+      for (int jq = 0; jq < Q; ++jq) {
+        const int64_t row = (static_cast<int64_t>(w1.b) * Q + jq) * p.Hq + w1.g * kGroup;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q + row * kHeadDim);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * lane));
+      }
+    }
     prepare_query_tile<kFp8Q, true>(p, w0.b, w0.g, qtiles, qtiles + qtile_half, qmul_ring, lane,
                                     first_tile_staging(G, kFp8Q, stages, qtiles), warp - 2, nq0);
     tc::fence_proxy_async_smem();   // read by the tensor core (and the staging rewritten by TMA)
@@ -429,6 +453,28 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     }
     named_barrier(2, kNumThreads - 64);  // no wait precedes it: warps 1 and 3+ all arrive
     all_valid = *reinterpret_cast<volatile int*>(&tail->any_invalid) == 0;
+  }
+
+  // A second unit near the start of the range: its tile by the query warp and
+  // the combiner warp (idle until the first page's maxima), after the check
+  // above, into the second buffer (the first tile's staging there has been
+  // read), rows read directly.  An fp8 query's tile is a plain copy, quick
+  // for the query warp alone.
+  if (!kFp8Q && !kWide && count > 0 && (warp == 2 || warp == 7)) {
+    PageWalk w1;
+    w1.begin(p, tail->start_b, tail->start_rem);
+    if (second_tile_early(G, w1, count)) {
+      w1.advance(p, w1.nhi - w1.n);
+      prepare_query_tile<kFp8Q, true>(p, w1.b, w1.g, qtiles + G.qtile_bytes,
+                                      qtiles + G.qtile_bytes + qtile_half, qmul_ring + Q, lane,
+                                      nullptr, warp == 2 ? 0 : 1, 2);
+      tc::fence_proxy_async_smem();
+      named_barrier(1, 64);
+      if (warp == 2 && lane == 0) {
+        mbar_arrive(&tail->qfull[1]);
+        mbar_arrive(&tail->qmul_ready[1]);
+      }
+    }
   }
 
   if (warp == 0) {
@@ -542,10 +588,11 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     // ---- query tiles, then the -inf tails ----------------------------------------------
     PageWalk w;
     if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
+    const bool pre1 = !kFp8Q && !kWide && count > 0 && second_tile_early(G, w, count);   // tile 1 built above
     int t = 0, k = 0;
     bool ok = true;
     while (t < count && ok) {
-      if (k > 0) {   // the first tile is built above
+      if (k > 0 && !(k == 1 && pre1)) {   // the first tile is built above
         const int qb = k % G.nqb;
         if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], ((k / G.nqb) - 1) & 1)) {
           if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
