@@ -244,7 +244,12 @@ int msa_sparse_decode_select(const void *q, const void *kv, const int32_t *block
  * min(16, ceil(S / 16)), each split a range of ceil(S / splits) consecutive
  * blocks.  Returns 0 when S < 1 or a range would exceed 128 blocks (S > 2048,
  * contexts beyond 256k tokens), which msa_dense_decode rejects.  Size its
- * workspace with msa_workspace_bytes(B, Q, Hq, msa_dense_splits(S)).
+ * workspace with msa_workspace_bytes(B, Q, Hq, msa_dense_splits(S)).  For
+ * Q >= 2 this is the most parts a row is cut into: when the (request,
+ * 4-token tile, KV head) units are fewer than the SMs, each unit takes a
+ * share of one CTA per SM in proportion to its visible blocks (computed on
+ * the device from seq_lens), up to this many; with as many units as SMs,
+ * one part each.
  */
 int msa_dense_splits(int S);
 
@@ -254,8 +259,9 @@ int msa_dense_splits(int S);
  * first layers attend the whole page table).  The same operation as
  * msa_sparse_decode with each row's list being all of its blocks 0 .. cur(i)
  * (keys 128 n + t <= pos(i)); no list is read.  Splits as msa_dense_splits;
- * with more than one the partials go to `workspace` and the merge is enqueued
- * on `stream`.  Numerics as msa_sparse_decode.
+ * with more than one the partials go to `workspace` (parts a row does not use
+ * are marked empty) and the merge is enqueued on `stream`.  Numerics as
+ * msa_sparse_decode.
  * Errors: as msa_sparse_decode (topk and num_splits aside), plus S > 2048
  * (MSA_EINVAL).  Device: MSA_ERR_PAGE_RANGE (page skipped), MSA_ERR_SEQ_RANGE.
  */
