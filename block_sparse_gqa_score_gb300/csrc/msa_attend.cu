@@ -144,7 +144,7 @@ __device__ __forceinline__ bool varlen_token(const int32_t* __restrict__ cu_q, i
 // query length per request (cu_q), grid.x = T tokens.  Each is compiled
 // separately so that the bf16 list-mode decode kernel carries none of their
 // branches.
-template <bool kDense, bool kFp8Q, bool kVarlen = false>
+template <bool kDense, bool kFp8Q, bool kVarlen = false, bool kListsOnly = false>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap kv_map, const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
       pdl_wait();  // the top-k lists, or the scores they come from, are the previous kernel's
       int n;
-      if (p.scores) {
+      if (!kListsOnly && p.scores) {
         // select this row's blocks here; stage 1, not yet loaded, is the scratch
         bool nan = false;
         uint8_t* scratch = smem + kStageBytes;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       // a block listed again at a later slot is dropped (a given list only: the
       // selector's lists hold distinct blocks)
-      const unsigned same = p.scores ? 0u : __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
+      const unsigned same = (!kListsOnly && p.scores) ? 0u : __match_any_sync(0xffffffffu, valid ? n : -2 - lane);
       if (valid && (same & ((1u << lane) - 1u))) {
         flag_error(p.err, MSA_ERR_TOPK_DUP);
         valid = false;
@@ -723,7 +723,8 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   cudaError_t e = once_per_device(attr_done, [] {
     for (auto* k : {attend_kernel<false, false>, attend_kernel<true, false>,
                     attend_kernel<false, true>, attend_kernel<true, true>,
-                    attend_kernel<false, false, true>, attend_kernel<false, true, true>}) {
+                    attend_kernel<false, false, true>, attend_kernel<false, true, true>,
+                    attend_kernel<false, false, false, true>, attend_kernel<false, true, false, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (r != cudaSuccess) return r;
@@ -745,13 +746,19 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
                              kv_map, p)
                 : launch_pdl(attend_kernel<false, false, true>, grid, block, kSmemBytes, stream, pdl,
                              kv_map, p);
+  // decode on given lists: an instantiation without the prologue's selector
+  const bool lists = p.scores == nullptr && p.dense_span == 0;
   if (p.q8)
     return p.dense_span > 0
                ? launch_pdl(attend_kernel<true, true>, grid, block, kSmemBytes, stream, pdl, kv_map, p)
-               : launch_pdl(attend_kernel<false, true>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
+           : lists ? launch_pdl(attend_kernel<false, true, false, true>, grid, block, kSmemBytes,
+                                stream, pdl, kv_map, p)
+                   : launch_pdl(attend_kernel<false, true>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
   return p.dense_span > 0
              ? launch_pdl(attend_kernel<true, false>, grid, block, kSmemBytes, stream, pdl, kv_map, p)
-             : launch_pdl(attend_kernel<false, false>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
+         : lists ? launch_pdl(attend_kernel<false, false, false, true>, grid, block, kSmemBytes,
+                              stream, pdl, kv_map, p)
+                 : launch_pdl(attend_kernel<false, false>, grid, block, kSmemBytes, stream, pdl, kv_map, p);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_ml, uint16_t* out, int64_t rows,
