@@ -724,7 +724,8 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
     for (auto* k : {attend_kernel<false, false>, attend_kernel<true, false>,
                     attend_kernel<false, true>, attend_kernel<true, true>,
                     attend_kernel<false, false, true>, attend_kernel<false, true, true>,
-                    attend_kernel<false, false, false, true>, attend_kernel<false, true, false, true>}) {
+                    attend_kernel<false, false, false, true>, attend_kernel<false, true, false, true>,
+                    attend_kernel<false, false, true, true>, attend_kernel<false, true, true, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (r != cudaSuccess) return r;
@@ -741,11 +742,17 @@ cudaError_t launch_attend(const CUtensorMap& kv_map, const AttendParams& p, cuda
   const int T = p.cu_q ? p.T : p.B * p.Q;
   dim3 grid(T, p.Hkv, p.splits);
   const dim3 block(kThreads);
-  if (p.cu_q)  // prefill-style batches take lists only (no dense mode)
+  if (p.cu_q) {  // prefill-style batches (no dense mode); given lists: no selector
+    if (p.scores == nullptr)
+      return p.q8 ? launch_pdl(attend_kernel<false, true, true, true>, grid, block, kSmemBytes,
+                               stream, pdl, kv_map, p)
+                  : launch_pdl(attend_kernel<false, false, true, true>, grid, block, kSmemBytes,
+                               stream, pdl, kv_map, p);
     return p.q8 ? launch_pdl(attend_kernel<false, true, true>, grid, block, kSmemBytes, stream, pdl,
                              kv_map, p)
                 : launch_pdl(attend_kernel<false, false, true>, grid, block, kSmemBytes, stream, pdl,
                              kv_map, p);
+  }
   // decode on given lists: an instantiation without the prologue's selector
   const bool lists = p.scores == nullptr && p.dense_span == 0;
   if (p.q8)
