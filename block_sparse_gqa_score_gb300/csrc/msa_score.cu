@@ -296,8 +296,10 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
 // is fp8 (q8 * q_scale), compiled separately so that the bf16 kernel carries
 // none of its branches.  kWide: the extra sets of epilogue warps (one CTA
 // per SM, 640 threads), likewise a separate instantiation; the launch bounds
-// keep 128 registers for the two-CTA kernel.
-template <bool kFp8Q, bool kWide>
+// keep 128 registers for the two-CTA kernel.  kFuse: a bf16 query's hi and lo
+// parts in one product (qlen <= 2, ScoreGeometry::fuse), its own
+// instantiation too, so that the qlen 3-8 kernel carries none of it.
+template <bool kFp8Q, bool kWide, bool kFuse = false>
 __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
   constexpr int kSub = kWide ? kWideSub : 1;              // epilogue warps per TMEM lane quarter
@@ -522,7 +524,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       const uint64_t lo_step = static_cast<uint64_t>(qtile_half >> 4);
       uint32_t idesc[2];
       for (int h = 0; h < 2; ++h)
-        idesc[h] = tc::idesc_e4m3_f32(128, (G.fuse ? 32 : 16) * max(1, min(G.Qu, Q - h * G.Qu)));
+        idesc[h] = tc::idesc_e4m3_f32(128, ((kWide ? G.fuse != 0 : kFuse) ? 32 : 16) *
+                                               max(1, min(G.Qu, Q - h * G.Qu)));
       PageWalk w;
       if (count > 0) w.begin(p, tail->start_b, tail->start_rem);
       int k = -1, pb = -1, pg = -1, vp = 0;
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
           const uint64_t bh = bq + static_cast<uint64_t>((h * G.Qu * kGroup * 128) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) tc::mma_e4m3(d, a + 2 * ks, bh + 2 * ks, idesc[h], ks > 0);
-          if (!kFp8Q && (kWide || !G.fuse)) {  // the lo part of a bf16 query adds into the same columns
+          if (!kFp8Q && (kWide ? !G.fuse : !kFuse)) {  // the lo part of a bf16 query adds into the same columns
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               tc::mma_e4m3(d, a + 2 * ks, bh + lo_step + 2 * ks, idesc[h], 1);
@@ -666,7 +669,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
         tc::fence_after_thread_sync();
         const int tok0 = h * G.Qu, ntok = min(G.Qu, Q - tok0);
         const uint32_t acc = lane_addr + buf * G.ucols;
-        if (!kFp8Q && !kWide && G.fuse) {   // (fused only at qlen <= 2: two CTAs per SM)
+        if (kFuse) {   // (fused only at qlen <= 2: two CTAs per SM)
           // token by token: its hi columns (16 j) and lo columns (16 Qu + 16 j),
           // summed head by head before the maximum
           for (int j = sub; j < ntok; j += kSub) {
@@ -785,7 +788,8 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
     for (auto* k : {score_kernel<false, false>, score_kernel<true, false>,
-                    score_kernel<false, true>, score_kernel<true, true>}) {
+                    score_kernel<false, true>, score_kernel<true, true>,
+                    score_kernel<false, false, true>}) {
       cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemLimit);
       if (r != cudaSuccess) return r;
@@ -802,8 +806,9 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   if (G.nsub > 1)   // the wide instantiation (kWide) is the one built for G.threads
     return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, pdl, kv_map, p)
                 : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, pdl, kv_map, p);
-  return p.q8 ? launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, pdl, kv_map, p)
-              : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, pdl, kv_map, p);
+  if (p.q8) return launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, pdl, kv_map, p);
+  return G.fuse ? launch_pdl(score_kernel<false, false, true>, grid, block, G.smem, stream, pdl, kv_map, p)
+                : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, pdl, kv_map, p);
 }
 
 }  // namespace msa
