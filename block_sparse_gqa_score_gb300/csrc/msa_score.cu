@@ -298,8 +298,13 @@ __device__ void prepare_query_tile(const ScoreParams& p, int b, int g, uint8_t* 
 // per SM, 640 threads), likewise a separate instantiation; the launch bounds
 // keep 128 registers for the two-CTA kernel.  kFuse: a bf16 query's hi and lo
 // parts in one product (qlen <= 2, ScoreGeometry::fuse), its own
-// instantiation too, so that the qlen 3-8 kernel carries none of it.
-template <bool kFp8Q, bool kWide, bool kFuse = false>
+// instantiation too, so that the qlen 3-8 kernel carries none of it.  kQ:
+// the query length as a compile-time constant (0: read from the arguments).
+// With it the whole geometry (stages, accumulator and tile buffers, token
+// groups) is constant, and the ring indices of the per-page loops divide by
+// constants instead of by runtime values: the qlen-4 scorer went from 39.9
+// to 31.6 us.  The common lengths are instantiated (see launch_score).
+template <bool kFp8Q, bool kWide, bool kFuse = false, int kQ = 0>
 __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     score_kernel(const __grid_constant__ CUtensorMap kv_map, const ScoreParams p) {
   constexpr int kSub = kWide ? kWideSub : 1;              // epilogue warps per TMEM lane quarter
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int Q = p.Q;
+  const int Q = kQ > 0 ? kQ : p.Q;   // kQ: the query length compiled in (0: the argument's)
   const ScoreGeometry G = score_geometry(Q, kFp8Q);
   uint8_t* stages = smem;                                              // [stages][128][128 B]
   uint8_t* qtiles = smem + G.off_q;                                    // [nqb][hi, lo][16Q][128 B]
@@ -780,6 +785,17 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
 
 }  // namespace
 
+// The instantiations: the bf16 qlen 3 and 4 and the fp8 qlen 4 two-CTA
+// kernels and the wide bf16 qlen 32 kernel with the query length compiled in
+// (measured: the qlen-4 scorer 39.9 -> 31.6 us, fp8 34.1 -> 31.7 us, qlen 32
+// 1574 -> 1362 us); the rest read it from the arguments, the fused qlen 1-2
+// path among them (with qlen 1 compiled in, batch 128 / qlen 1 ran 263.2
+// instead of 256.7 us).
+#define MSA_SCORE_KERNELS(X)                                                                    \
+  X(false, false, true, 0) X(false, false, false, 3) X(false, false, false, 4)                  \
+  X(false, false, false, 0) X(true, false, false, 4) X(true, false, false, 0)                   \
+  X(false, true, false, 32) X(false, true, false, 0) X(true, true, false, 0)
+
 cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream,
                          bool pdl) {
   if (p.ctas < 1) return cudaErrorInvalidValue;
@@ -787,28 +803,32 @@ cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaSt
   if (G.stages < 2 || G.smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    for (auto* k : {score_kernel<false, false>, score_kernel<true, false>,
-                    score_kernel<false, true>, score_kernel<true, true>,
-                    score_kernel<false, false, true>}) {
-      cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemLimit);
-      if (r != cudaSuccess) return r;
-      // all of the unified L1 / shared storage as shared memory, so that two
-      // CTAs of ~100 KB can be resident on one SM
-      r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
-      if (r != cudaSuccess) return r;
+#define MSA_SET_ATTR(F8, W, FU, QQ)                                                              \
+    {                                                                                          \
+      auto* k = score_kernel<F8, W, FU, QQ>;                                                   \
+      cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                           kSmemLimit);                                        \
+      if (r != cudaSuccess) return r;                                                          \
+      r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,              \
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));              \
+      if (r != cudaSuccess) return r;                                                          \
     }
+    // all of the unified L1 / shared storage as shared memory, so that two
+    // CTAs of ~100 KB can be resident on one SM
+    MSA_SCORE_KERNELS(MSA_SET_ATTR)
+#undef MSA_SET_ATTR
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
   const dim3 grid(p.ctas * G.per_sm), block(G.threads);
-  if (G.nsub > 1)   // the wide instantiation (kWide) is the one built for G.threads
-    return p.q8 ? launch_pdl(score_kernel<true, true>, grid, block, G.smem, stream, pdl, kv_map, p)
-                : launch_pdl(score_kernel<false, true>, grid, block, G.smem, stream, pdl, kv_map, p);
-  if (p.q8) return launch_pdl(score_kernel<true, false>, grid, block, G.smem, stream, pdl, kv_map, p);
-  return G.fuse ? launch_pdl(score_kernel<false, false, true>, grid, block, G.smem, stream, pdl, kv_map, p)
-                : launch_pdl(score_kernel<false, false>, grid, block, G.smem, stream, pdl, kv_map, p);
+  const bool f8 = p.q8 != nullptr, wide = G.nsub > 1, fuse = G.fuse != 0;
+#define MSA_LAUNCH_IF(F8, W, FU, QQ)                                                             \
+  if (f8 == F8 && wide == W && fuse == FU && (QQ == 0 || p.Q == QQ))                            \
+    return launch_pdl(score_kernel<F8, W, FU, QQ>, grid, block, G.smem, stream, pdl, kv_map, p);
+  // the instantiations with the length compiled in come before the generic ones
+  MSA_SCORE_KERNELS(MSA_LAUNCH_IF)
+#undef MSA_LAUNCH_IF
+  return cudaErrorInvalidValue;   // unreachable: every (fp8, wide, fused) has a generic kernel
 }
 
 }  // namespace msa
