@@ -785,16 +785,23 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
 
 }  // namespace
 
-// The instantiations: the bf16 qlen 3 and 4 and the fp8 qlen 4 two-CTA
-// kernels and the wide bf16 qlen 32 kernel with the query length compiled in
-// (measured: the qlen-4 scorer 39.9 -> 31.6 us, fp8 34.1 -> 31.7 us, qlen 32
-// 1574 -> 1362 us); the rest read it from the arguments, the fused qlen 1-2
-// path among them (with qlen 1 compiled in, batch 128 / qlen 1 ran 263.2
-// instead of 256.7 us).
+// The instantiations with the query length compiled in: bf16 qlen 3-7 and
+// fp8 qlen 1-7 (two CTAs per SM), bf16 and fp8 qlen 8, 16 and 32 (one CTA per
+// SM).  Measured at batch 16 over 8k-32k tokens, generic -> compiled in: bf16
+// qlen 4 39.9 -> 31.6 us, 5 52.1 -> 40.8, 8 87.5 -> 67.7, 16 116.3 -> 95.7,
+// 32 1574 -> 1362 (the qlen-32 workload); fp8 qlen 4 34.1 -> 31.7, 5 47.2 ->
+// 35.0, 8 67.6 -> 52.8, 16 88.9 -> 69.6.  The other lengths read it from the
+// arguments, and so does the fused bf16 qlen 1-2 path (with qlen 1 compiled
+// in, batch 128 / qlen 1 ran 263.2 instead of 256.7 us).
 #define MSA_SCORE_KERNELS(X)                                                                    \
   X(false, false, true, 0) X(false, false, false, 3) X(false, false, false, 4)                  \
-  X(false, false, false, 0) X(true, false, false, 4) X(true, false, false, 0)                   \
-  X(false, true, false, 32) X(false, true, false, 0) X(true, true, false, 0)
+  X(false, false, false, 5) X(false, false, false, 6) X(false, false, false, 7)                 \
+  X(false, false, false, 0) X(true, false, false, 1) X(true, false, false, 2)                   \
+  X(true, false, false, 3) X(true, false, false, 4) X(true, false, false, 5)                    \
+  X(true, false, false, 6) X(true, false, false, 7) X(true, false, false, 0)                    \
+  X(false, true, false, 8) X(false, true, false, 16) X(false, true, false, 32)                  \
+  X(false, true, false, 0) X(true, true, false, 8) X(true, true, false, 16)                   \
+  X(true, true, false, 32) X(true, true, false, 0)
 
 cudaError_t launch_score(const CUtensorMap& kv_map, const ScoreParams& p, cudaStream_t stream,
                          bool pdl) {
