@@ -403,6 +403,32 @@ def test_fp8_query_matches_oracle(seq_lens, Q, Hq, Hkv):
     assert msa.get_error() == 0
 
 
+# Every query length the scorer has its own instantiation for (the length
+# compiled in), and a generic one on each side of them, bf16 and fp8: the
+# two-CTA kernels up to qlen 7, the one-CTA kernels from qlen 8.
+SCORE_QLENS = [(q, fp8) for q in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 17, 32) for fp8 in (False, True)]
+
+
+@pytest.mark.parametrize("Q,fp8", SCORE_QLENS)
+def test_score_every_compiled_query_length(Q, fp8):
+    """Scores against the oracle for each query length the scorer compiles in
+    (and generic neighbours), with a bf16 or an fp8 query; rows straddle a
+    unit boundary near the start of a CTA's range (short and long requests)."""
+    seq_lens, Hq, Hkv = [700, 5000, 129, 2300], 32, 2
+    inp = wl.make_custom(seq_lens, Q, Hq, Hkv, seed=140 + Q, device=DEV, kv_std=0.5,
+                         kv_scale_mode="amax")
+    if fp8:
+        q8, qs, p = _fp8_query(inp)
+        gpu = msa.score(q8, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale, inp.k_scale,
+                        q_scale=qs)
+    else:
+        p = to_problem(inp, oracle)
+        gpu = msa.score(inp.q, inp.kv, inp.block_table, inp.seq_lens, Q, inp.sm_scale,
+                        inp.k_scale)
+    assert_scores_close(_np(gpu).astype(np.float64), oracle.score(p))
+    assert msa.get_error() == 0
+
+
 def test_dense_decode_skips_and_flags_a_bad_page():
     """A block-table entry out of range in dense decode: that block is skipped
     and MSA_ERR_PAGE_RANGE set; the rest equals the oracle over every other
