@@ -315,6 +315,40 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
                                              ~static_cast<uintptr_t>(1023));
   const int Q = kQ > 0 ? kQ : p.Q;   // kQ: the query length compiled in (0: the argument's)
   const ScoreGeometry G = score_geometry(Q, kFp8Q);
+  // Ring indices of the per-page loops: with the length compiled in the
+  // divisors are constants; otherwise the stage count (2-8) divides through
+  // a multiply-high by ceil(2^32 / stages) (exact for indices below 2^29),
+  // and the accumulator and tile buffer counts (powers of two) by shifts
+  // (generic qlen 9-24 scorers 9-15 % faster).  The fused qlen 1-2 kernel
+  // keeps plain divisions: like this, or with qlen 1 compiled in, batch 128 /
+  // qlen 1 ran 269 and 263 instead of 257 us.
+  constexpr bool kPlainDiv = kQ > 0 || kFuse;
+  const uint32_t st_magic = kPlainDiv ? 0u : static_cast<uint32_t>(0xFFFFFFFFull / G.stages + 1);
+  const int acc_sh = G.nacc == 4 ? 2 : 1, qb_sh = G.nqb == 2 ? 1 : 0;
+  auto st_div = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x / G.stages;
+    else return static_cast<int>(__umulhi(static_cast<uint32_t>(x), st_magic));
+  };
+  auto st_mod = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x % G.stages;
+    else return x - st_div(x) * G.stages;
+  };
+  auto acc_div = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x / G.nacc;
+    else return x >> acc_sh;
+  };
+  auto acc_mod = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x % G.nacc;
+    else return x & (G.nacc - 1);
+  };
+  auto qb_div = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x / G.nqb;
+    else return x >> qb_sh;
+  };
+  auto qb_mod = [&](int x) -> int {
+    if constexpr (kPlainDiv) return x % G.nqb;
+    else return x & (G.nqb - 1);
+  };
   uint8_t* stages = smem;                                              // [stages][128][128 B]
   uint8_t* qtiles = smem + G.off_q;                                    // [nqb][hi, lo][16Q][128 B]
   float* qmul_ring = reinterpret_cast<float*>(smem + G.off_qmul);      // [kQmulRing][Q]
@@ -497,8 +531,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
           if (p.err) flag_error(p.err, MSA_ERR_PAGE_RANGE);
           continue;
         }
-        const int s = vp % G.stages;
-        if (vp >= G.stages && !mbar_wait(&tail->empty[s], ((vp / G.stages) - 1) & 1)) {
+        const int s = st_mod(vp);
+        if (vp >= G.stages && !mbar_wait(&tail->empty[s], (st_div(vp) - 1) & 1)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
@@ -514,7 +548,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       }
       // the last loads in flight land before shared memory can be released
       for (int t = vp - G.stages; t < vp; ++t)
-        if (t >= 0) (void)mbar_wait(&tail->full[t % G.stages], (t / G.stages) & 1);
+        if (t >= 0) (void)mbar_wait(&tail->full[st_mod(t)], st_div(t) & 1);
       // every load of this CTA has landed: the next kernel may start its CTAs
       pdl_trigger();
       mbar_arrive(&tail->finish);
@@ -537,7 +571,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       bool q_ready = false, ok = true;
       for (int t = 0; t < count && ok; ++t, w.next(p)) {
         if (w.b != pb || w.g != pg) {
-          if (k >= 0) tc::commit(&tail->qempty[k % G.nqb]);  // old tile free once its MMAs end
+          if (k >= 0) tc::commit(&tail->qempty[qb_mod(k)]);  // old tile free once its MMAs end
           ++k;
           pb = w.b;
           pg = w.g;
@@ -546,23 +580,23 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
         int page;
         if (!all_valid && !page_valid(p, w, page)) continue;
         if (!q_ready) {
-          if (!mbar_wait(&tail->qfull[k % G.nqb], (k / G.nqb) & 1)) {
+          if (!mbar_wait(&tail->qfull[qb_mod(k)], qb_div(k) & 1)) {
             flag_error(p.err, MSA_ERR_TIMEOUT);
             break;
           }
           tc::fence_after_thread_sync();
           q_ready = true;
         }
-        const int s = vp % G.stages;
-        if (!mbar_wait(&tail->full[s], (vp / G.stages) & 1)) {
+        const int s = st_mod(vp);
+        if (!mbar_wait(&tail->full[s], st_div(vp) & 1)) {
           flag_error(p.err, MSA_ERR_TIMEOUT);
           break;
         }
         tc::fence_after_thread_sync();
         const uint64_t a = adesc0 + static_cast<uint64_t>(s) * (kHalfTile >> 4);
-        const uint64_t bq = bdesc0 + static_cast<uint64_t>((k % G.nqb) * (G.qtile_bytes >> 4));
+        const uint64_t bq = bdesc0 + static_cast<uint64_t>(qb_mod(k) * (G.qtile_bytes >> 4));
         for (int h = 0; h < G.nh; ++h) {
-          const int u = vp * G.nh + h, buf = u % G.nacc, use = u / G.nacc;
+          const int u = vp * G.nh + h, buf = acc_mod(u), use = acc_div(u);
           if (use >= 1) {
             if (!mbar_wait(&tail->dempty[buf], (use - 1) & 1)) {
               flag_error(p.err, MSA_ERR_TIMEOUT);
@@ -601,8 +635,8 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
     bool ok = true;
     while (t < count && ok) {
       if (k > 0 && !(k == 1 && pre1)) {   // the first tile is built above
-        const int qb = k % G.nqb;
-        if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], ((k / G.nqb) - 1) & 1)) {
+        const int qb = qb_mod(k);
+        if (k >= G.nqb && !mbar_wait(&tail->qempty[qb], (qb_div(k) - 1) & 1)) {
           if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
           ok = false;
           break;
@@ -665,7 +699,7 @@ __global__ void __launch_bounds__(kWide ? 640 : 256, kWide ? 1 : 2)
       const int lim_base = w.L - Q - w.n * kPage;   // token j sees keys <= lim_base + j
       float myv = -INFINITY;                        // lane jq: this quarter's max of token jq
       for (int h = 0; h < G.nh && ok; ++h) {
-        const int u = vp * G.nh + h, buf = u % G.nacc, use = u / G.nacc;
+        const int u = vp * G.nh + h, buf = acc_mod(u), use = acc_div(u);
         if (!mbar_wait(&tail->dfull[buf], use & 1)) {
           if (lane == 0) flag_error(p.err, MSA_ERR_TIMEOUT);
           ok = false;
